@@ -1,0 +1,501 @@
+"""Bench: achieved HBM GB/s of the fused epilogue ops on GB300.
+
+One step = one call of every op on its measured workload (SkipLayerNormalization
+f16 16384x4096 with bias/residual, f32 (32,2048,1024) with a broadcast skip and
+f32 (2,128,768); BiasSoftmax f16 (32,16,512,512) causal, f32 64x262144 and
+8x1048576 long rows; BiasAdd f16 (16,1024,4096); QuickGelu f16 67,108,867).
+
+value        = minimum bytes of all ops (every input read once, every output
+               written once, reused vectors counted once) / device time of a step
+e2e          = the same metric with each step's inputs copied host->device from
+               pinned memory and outputs copied back, inside the timed region
+roofline     = the dominant kernel's algorithmic bytes / its mean CUDA-event
+               duration, against the measured HBM copy bandwidth
+cpu_baseline = the float64 CPU oracle on a bounded sample of the same workloads
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same workloads on its own GPU
+(independent replicas: the ops are row-independent and need no exchange);
+timings are max-reduced over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gen import synth  # noqa: E402
+
+METRIC = "achieved HBM GB/s per op and % of GB300 HBM roofline; rows/sec for SkipLayerNorm"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+# Step order: each small workload follows a large streaming one.
+ORDER = [
+    "sln_f16_16384x4096_bias_residual",
+    "sln_f32_2x128x768",
+    "sln_f32_32x2048x1024_bcast_skip",
+    "bias_add_f16_16x1024x4096",
+    "bias_softmax_f32_64x262144_cyclic",
+    "quick_gelu_f16_67108867",
+    "bias_softmax_f16_32x16x512x512_causal",
+    "bias_softmax_f32_8x1048576",
+]
+
+# DRAM bytes (read + write) per launch from ncu captures, keyed by workload,
+# with the hash of the kernel sources they were taken on.  A changed source
+# makes the figure stale and it is reported as null.
+NCU_TRAFFIC = {}
+NCU_TRAFFIC_SOURCE_HASH = None
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "transformer_epilogue_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------
+# workloads: minimum bytes and calls
+# ---------------------------------------------------------------------------
+
+def nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def min_bytes(name, d):
+    """Every input read once, every output written once; reused vectors
+    (gamma, beta, bias, a broadcast skip, bias rows) count once."""
+    w = synth.WORKLOADS[name]
+    if w.op == "skip_layer_norm":
+        b = sum(nbytes(d[k]) for k in ("input", "skip", "gamma", "beta", "bias"))
+        b += nbytes(d["input"]) * (2 if d.get("residual") else 1)
+        return b
+    if w.op == "bias_softmax":
+        return nbytes(d["data"]) * 2 + nbytes(d["bias"])
+    if w.op == "bias_add":
+        return nbytes(d["X"]) * 2 + nbytes(d["skip"]) + nbytes(d["bias"])
+    if w.op == "quick_gelu":
+        return nbytes(d["X"]) * 2
+    raise KeyError(name)
+
+
+def rows_of(name, d):
+    w = synth.WORKLOADS[name]
+    if w.op == "skip_layer_norm":
+        return d["input"].numel() // d["input"].shape[-1]
+    return None
+
+
+class DeviceWorkload:
+    """Device-resident inputs/outputs of one workload and its op call."""
+
+    def __init__(self, name, host, device):
+        import transformer_epilogue_gb300 as te
+        self.te = te
+        self.name = name
+        self.op = synth.WORKLOADS[name].op
+        self.host = host
+        self.dev = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+        d = self.dev
+        if self.op == "skip_layer_norm":
+            self.outs = {"output": torch.empty_like(d["input"])}
+            if host.get("residual"):
+                self.outs["sum"] = torch.empty_like(d["input"])
+        elif self.op == "bias_softmax":
+            self.outs = {"output": torch.empty_like(d["data"])}
+            need = te.ep_bias_softmax_workspace_size(d["data"].dtype, d["data"].shape, d["axis"])
+            self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device) if need else None
+        else:
+            self.outs = {"Y": torch.empty_like(d["X"])}
+        self.inputs = [k for k, v in self.dev.items() if isinstance(v, torch.Tensor)]
+
+    def call(self):
+        te, d, o = self.te, self.dev, self.outs
+        if self.op == "skip_layer_norm":
+            te.ep_skip_layer_norm(d["input"], d["skip"], d["gamma"], d["beta"], d["bias"], d["epsilon"],
+                                  output=o["output"], input_skip_bias_sum=o.get("sum"))
+        elif self.op == "bias_softmax":
+            te.ep_bias_softmax(d["data"], d["bias"], axis=d["axis"], is_inner_broadcast=d["is_inner_broadcast"],
+                               output=o["output"], workspace=self.ws)
+        elif self.op == "bias_add":
+            te.ep_bias_add(d["X"], d["bias"], d["skip"], Y=o["Y"])
+        else:
+            te.ep_quick_gelu(d["X"], d["alpha"], Y=o["Y"])
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.idx)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        self.t0 = time.time()
+
+    def mark(self):
+        return time.time()
+
+    def stop(self, t_begin, t_end):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+            except (ValueError, IndexError):
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        inside = [r for r in rows if t_begin - 0.15 <= r[0] <= t_end + 0.15] or rows
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            for n, v in zip(names, r[3][1:5]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on bounded samples (the cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_call(name, d, frac_rows):
+    """Run the oracle on the first max(1, frac_rows * rows) rows of a workload;
+    returns the minimum bytes of that sample."""
+    import oracle
+    w = synth.WORKLOADS[name]
+    if w.op == "skip_layer_norm":
+        H = d["input"].shape[-1]
+        R = d["input"].numel() // H
+        n = max(1, int(R * frac_rows))
+        rows = list(range(n))
+        oracle.skip_layer_norm(d["input"], d["skip"], d["gamma"], d["beta"], d["bias"], d["epsilon"], rows=rows)
+        if d.get("residual"):
+            oracle.skip_bias_sum(d["input"], d["skip"], d["bias"], rows=rows)
+        es = d["input"].element_size()
+        return n * H * es * (3 + (1 if d.get("residual") else 0))
+    if w.op == "bias_softmax":
+        dims = oracle.bias_softmax_dims(tuple(d["data"].shape), d["bias"].numel(), d["axis"])
+        n = max(1, int(dims["batch"] * frac_rows))
+        oracle.bias_softmax(d["data"], d["bias"], d["axis"], d["is_inner_broadcast"], rows=list(range(n)))
+        return n * dims["block"] * d["data"].element_size() * 3
+    if w.op == "bias_add":
+        C = d["X"].shape[-1]
+        R = d["X"].numel() // C
+        n = max(1, int(R * frac_rows))
+        X = d["X"].reshape(-1, C)[:n].reshape(1, n, C)
+        S = d["skip"].reshape(-1, C)[:n].reshape(1, n, C)
+        oracle.bias_add(X, d["bias"], S)
+        return n * C * d["X"].element_size() * 3
+    n = max(1, int(d["X"].numel() * frac_rows))
+    oracle.quick_gelu(d["X"][:n], d["alpha"])
+    return n * d["X"].element_size() * 2
+
+
+def oracle_step(hosts, frac):
+    t0 = time.perf_counter()
+    b = sum(oracle_sample_call(n, hosts[n], frac) for n in ORDER)
+    return b, time.perf_counter() - t0
+
+
+def pin_one_core():
+    try:
+        cpu = sorted(os.sched_getaffinity(0))[0]
+        old = os.sched_getaffinity(0)
+        os.sched_setaffinity(0, {cpu})
+        return old
+    except (AttributeError, OSError):
+        return None
+
+
+def cpu_baseline(hosts, budget_s=15.0):
+    old = pin_one_core()
+    try:
+        frac = 1.0 / 4096
+        b, t = oracle_step(hosts, frac)           # calibration
+        frac = min(1.0, frac * max(1.0, budget_s / max(t, 1e-3)))
+        b, t = oracle_step(hosts, frac)
+    finally:
+        if old is not None:
+            os.sched_setaffinity(0, old)
+    return {"value": b / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {frac:.5f} of the rows of every workload (numpy float64, 1 pinned core), "
+                      f"{b / 1e6:.1f} MB of minimum traffic in {t:.1f} s; host has {os.cpu_count()} cores"}
+
+
+# ---------------------------------------------------------------------------
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs: torch copy, read+write, burst)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, no MEASURED_PEAKS.json)"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max_sum(values_max, values_sum, ws):
+    """max over ranks of the first list, sum over ranks of the second."""
+    if ws == 1:
+        return list(values_max), list(values_sum)
+    import torch.distributed as dist
+    dev = torch.device("cuda") if dist.get_backend() == "nccl" else torch.device("cpu")
+    a = torch.tensor(values_max, dtype=torch.float64, device=dev)
+    b = torch.tensor(values_sum, dtype=torch.float64, device=dev)
+    dist.all_reduce(a, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return a.cpu().tolist(), b.cpu().tolist()
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def build_hosts():
+    hosts = {}
+    for n in ORDER:
+        hosts[n] = synth.workload(n)
+    return hosts
+
+
+def run_reference(args, ws, rank):
+    """The reference arm: the float64 CPU oracle, as it stands, on bounded
+    samples of the same workloads (rank 0 only)."""
+    if rank != 0:
+        return 0
+    hosts = build_hosts()
+    total_steps = args.steps + args.warmup
+    budget = min(2.0, 150.0 / max(1, total_steps))
+    old = pin_one_core()
+    try:
+        frac = 1.0 / 8192
+        _, t = oracle_step(hosts, frac)
+        frac = min(1.0, frac * max(0.05, budget / max(t, 1e-3)))
+        for _ in range(args.warmup):
+            oracle_step(hosts, frac)
+        tb, tt = 0, 0.0
+        for _ in range(args.steps):
+            b, t = oracle_step(hosts, frac)
+            tb += b
+            tt += t
+    finally:
+        if old is not None:
+            os.sched_setaffinity(0, old)
+    v = tb / tt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; gen/synth.py)",
+            "config": {"workload": "all eight epilogue workloads (bounded row samples on the CPU)",
+                       "sample_fraction_of_rows": frac},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"first {frac:.6f} of the rows of every workload per step"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if args.impl == "reference":
+        rc = run_reference(args, ws, rank)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return rc
+
+    import transformer_epilogue_gb300 as te
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    te.load_library()
+    hosts = build_hosts()
+    work = [DeviceWorkload(n, hosts[n], device) for n in ORDER]
+    bytes_per = [min_bytes(n, hosts[n]) for n in ORDER]
+    step_bytes = sum(bytes_per)
+    stream = torch.cuda.current_stream(device)
+
+    # warm-up
+    for _ in range(args.warmup):
+        for w in work:
+            w.call()
+    torch.cuda.synchronize()
+
+    # timed region: K steps, per-op events on the launching stream
+    K = args.steps
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in work]
+          for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    n_launch0 = te.kernel_launch_count()
+    wall0 = time.time()
+    t_start.record(stream)
+    for k in range(K):
+        for i, w in enumerate(work):
+            ev[k][i][0].record(stream)
+            w.call()
+            ev[k][i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier(ws)
+    launches = te.kernel_launch_count() - n_launch0
+    clk = clocks.stop(wall0, wall1)
+    total_ms = t_start.elapsed_time(t_end)
+    per_op_ms = [statistics.fmean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(K)) for i in range(len(work))]
+
+    # e2e: pinned host inputs -> device, op, outputs -> pinned host, per step
+    pinned_in = [{k: hosts[n][k].pin_memory() for k in w.inputs} for n, w in zip(ORDER, work)]
+    pinned_out = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in w.outs.items()} for w in work]
+    h2d = sum(nbytes(t) for p in pinned_in for t in p.values())
+    d2h = sum(nbytes(t) for p in pinned_out for t in p.values())
+
+    def e2e_step():
+        for w, pi, po in zip(work, pinned_in, pinned_out):
+            for k, t in pi.items():
+                w.dev[k].copy_(t, non_blocking=True)
+            w.call()
+            for k, t in po.items():
+                t.copy_(w.outs[k], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = e0.elapsed_time(e1)
+
+    [total_ms, e2e_ms], [units, e2e_units] = reduce_max_sum(
+        [total_ms, e2e_ms], [step_bytes * K, step_bytes * args.e2e_steps], ws)
+    if rank != 0:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_src = measured_peak()
+    value = units / (total_ms / 1e3) / 1e9
+    ops = {}
+    for n, b, ms in zip(ORDER, bytes_per, per_op_ms):
+        gbs = b / (ms / 1e3) / 1e9
+        o = {"us": ms * 1e3, "min_bytes": b, "gbs": gbs, "frac_of_measured_peak": gbs / peak}
+        r = rows_of(n, hosts[n])
+        if r:
+            o["rows_per_s"] = r / (ms / 1e3)
+        ops[n] = o
+    dom = max(range(len(ORDER)), key=lambda i: per_op_ms[i])
+    dom_name = ORDER[dom]
+    achieved = bytes_per[dom] / (per_op_ms[dom] / 1e3) / 1e9
+    src_hash = kernel_source_hash()
+    traffic = NCU_TRAFFIC.get(dom_name) if NCU_TRAFFIC_SOURCE_HASH == src_hash else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded normal/uniform draws and a causal mask; gen/synth.py)",
+        "config": {"workload": "one call of each epilogue op per step: " + ", ".join(ORDER),
+                   "step_min_bytes": step_bytes, "l2": "inputs larger than L2 (2.8 GB per step; each op "
+                   "streams buffers disjoint from the previous op's)", "parallelism": f"replicas x{ws}"},
+        "frac_of_measured_peak": value / peak,
+        "ops": ops,
+        "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src},
+        "e2e": {"value": e2e_units / (e2e_ms / 1e3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "kernel_source_hash": src_hash,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(hosts)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,185 @@
+/*
+ * transformer_epilogue_gb300 — C ABI of the fused transformer-block epilogue ops
+ * (SkipLayerNormalization, BiasSoftmax, BiasAdd, QuickGelu) for one NVIDIA GB300
+ * (sm_103a) GPU.
+ *
+ * The ops are the com.microsoft ONNX Runtime contrib ops whose definitions are
+ * given by the manifest pages "com.microsoft.SkipLayerNormalization",
+ * "com.microsoft.BiasSoftmax", "com.microsoft.BiasAdd" and
+ * "com.microsoft.QuickGelu" (sections `description`, `inputs`, `outputs`,
+ * `attributes`, `derive`).  Each entry point below cites the section that
+ * defines what it computes.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are dense, contiguous, row-major device buffers of element type T
+ *    (ep_dtype); every pointer is a device pointer owned by the caller.  The
+ *    library allocates nothing and frees nothing.
+ *  - Every call is asynchronous: it validates on the host, enqueues its kernel(s)
+ *    on `stream` and returns without synchronising.  Outputs are valid once the
+ *    stream reaches that point.  A NULL stream is the legacy default stream.
+ *  - All validation happens before anything is enqueued.  A contract violation
+ *    returns EP_ERR_INVALID_ARG, a legal op this library does not implement
+ *    (another element type, an unsupported rank) returns EP_ERR_UNSUPPORTED, a
+ *    split-row BiasSoftmax without enough workspace returns EP_ERR_WORKSPACE, and
+ *    a launch error reported by the CUDA runtime returns EP_ERR_CUDA.  On any
+ *    non-OK status nothing has been enqueued, except for EP_ERR_CUDA (the
+ *    runtime's state is then whatever the failing launch left).  ep_last_error()
+ *    gives a message for the calling thread's last non-OK status.
+ *  - Empty tensors (numel 0) return EP_OK without launching anything; their
+ *    pointers may be NULL.
+ *  - Pointers must be aligned to sizeof(T).  16-byte alignment is not
+ *    required: it selects the 128-bit vector path, and other alignments take a
+ *    scalar path with the same results.
+ *  - An output may alias an input exactly (same address, same size: in place).
+ *    Any other overlap between an output and another operand is rejected.
+ *  - Counts and offsets are 64-bit.
+ *  - Arithmetic is float32 for both element types; float16 results are
+ *    rounded once, to nearest-even, when stored.
+ */
+#ifndef TRANSFORMER_EPILOGUE_EP_H
+#define TRANSFORMER_EPILOGUE_EP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream; the same type as cudaStream_t (struct CUstream_st*). */
+typedef struct CUstream_st* ep_stream_t;
+
+/* Element type T.  The op definitions' typeConstraints list float32 and
+ * float16 (typeConstraints of all four manifests). */
+typedef enum { EP_F32 = 0, EP_F16 = 1 } ep_dtype;
+
+typedef enum {
+  EP_OK = 0,
+  EP_ERR_INVALID_ARG = 1,   /* shape, attribute, pointer or overlap contract violated   */
+  EP_ERR_UNSUPPORTED = 2,   /* legal for the op, not implemented here (dtype, rank)     */
+  EP_ERR_WORKSPACE = 3,     /* split-row BiasSoftmax: workspace NULL or too small       */
+  EP_ERR_CUDA = 4           /* the CUDA runtime reported an error for a launch          */
+} ep_status;
+
+/* Message for the calling thread's last non-OK status ("" if none).  The string
+ * belongs to the library and stays valid until the thread's next call. */
+const char* ep_last_error(void);
+
+/* Name of a status code, e.g. "EP_ERR_INVALID_ARG". */
+const char* ep_status_name(ep_status s);
+
+/* Number of kernels this library has enqueued in this process (all threads). */
+uint64_t ep_kernel_launch_count(void);
+
+/* Version of this ABI (incremented on any incompatible change). */
+int ep_abi_version(void);
+
+/*
+ * SkipLayerNormalization
+ *   com.microsoft.SkipLayerNormalization manifest: `description`, `inputs`,
+ *   `outputs`, `attributes.epsilon`, `derive.rank2CoreContract`,
+ *   `derive.broadcastSkipShapeOk`.
+ *
+ *   s = (input + skip) + bias          (float32, in this order; bias optional)
+ *   input_skip_bias_sum = T(s)         (optional output)
+ *   mu = mean(s), var = mean((s-mu)^2) over the last (hidden) axis, population
+ *   output = (s - mu) / sqrt(var + epsilon) * gamma + beta   (beta optional)
+ *
+ * input      [in_rank dims], in_rank 2 (rows, H) or 3 (N, S, H); H > 0.
+ * skip       rank 2: the shape of input.  rank-3 input: the shape of input,
+ *            (1, S, H) or (S, H); row r of input uses skip row r mod skipRows,
+ *            skipRows = numel(skip) / H.
+ * gamma      H elements (required).  beta, bias: H elements or NULL.
+ * epsilon    >= 0 (the op's default is 9.999999960041972e-13, float32 1e-12).
+ * output     shape of input.
+ * input_skip_bias_sum   shape of input, or NULL.
+ *
+ * Errors: EP_ERR_UNSUPPORTED for a dtype other than EP_F32/EP_F16 or a rank
+ * other than 2/3; EP_ERR_INVALID_ARG for a non-positive H, a skip shape not
+ * listed above, a negative or NaN epsilon, a NULL required pointer, a
+ * misaligned pointer or an overlap other than exact in-place aliasing.
+ */
+ep_status ep_skip_layer_norm(ep_dtype t,
+                             const void* input, const int64_t* in_shape, int in_rank,
+                             const void* skip, const int64_t* skip_shape, int skip_rank,
+                             const void* gamma, const void* beta, const void* bias,
+                             float epsilon,
+                             void* output, void* input_skip_bias_sum,
+                             ep_stream_t stream);
+
+/*
+ * BiasSoftmax
+ *   com.microsoft.BiasSoftmax manifest: `description`, `attributes.axis`,
+ *   `attributeDescriptions.is_inner_broadcast`, `derive` (axisNorm, batchCount,
+ *   blockSize, biasBlockCount, biasContract).
+ *
+ *   axisN = axis < 0 ? axis + rank : axis           (0 <= axisN < rank)
+ *   batchCount = prod(shape[0:axisN]); blockSize = prod(shape[axisN:rank])
+ *   biasRows = bias_numel / blockSize; innerRepeat = batchCount / biasRows
+ *   bias row of data row r: r / innerRepeat if is_inner_broadcast != 0,
+ *                           r % biasRows    otherwise
+ *   output[r, :] = softmax(data[r, :] + bias[bias row, :])
+ *
+ * data, output  `rank` dims given by `shape` (1 <= rank <= 16).
+ * bias          bias_numel elements; only its element count matters.
+ * The biasContract must hold: bias_numel % blockSize == 0,
+ * 0 < biasRows <= batchCount and batchCount % biasRows == 0, or data and bias
+ * are both empty.
+ * workspace     device scratch for rows too long to keep on chip (the split-row
+ *               path); ep_bias_softmax_workspace_size() gives the bytes needed
+ *               (0 when the row path is taken; then workspace may be NULL).
+ *               16-byte aligned; its contents on entry do not matter.
+ *
+ * Errors: EP_ERR_INVALID_ARG for an axis out of range, a violated biasContract,
+ * NULL/misaligned pointers or overlaps; EP_ERR_WORKSPACE when the split-row
+ * path needs more than workspace_bytes or workspace is NULL/misaligned.
+ */
+ep_status ep_bias_softmax(ep_dtype t,
+                          const void* data, const int64_t* shape, int rank,
+                          const void* bias, int64_t bias_numel,
+                          int axis, int is_inner_broadcast,
+                          void* output,
+                          void* workspace, size_t workspace_bytes,
+                          ep_stream_t stream);
+
+/* Workspace bytes ep_bias_softmax needs for this dtype, shape and axis (0 if
+ * none).  Returns 0 as well for arguments ep_bias_softmax would reject. */
+size_t ep_bias_softmax_workspace_size(ep_dtype t, const int64_t* shape, int rank, int axis);
+
+/*
+ * BiasAdd
+ *   com.microsoft.BiasAdd manifest: `description`, `inputs`, `outputs`.
+ *
+ *   Y[n, s, c] = (X[n, s, c] + bias[c]) + skip[n, s, c]
+ *
+ * shape   3 dims (N, S, C) of X, skip and Y; bias has C elements.
+ * For float32 the three-term sum is compensated (error-free two-sums), so Y
+ * is within one rounding of the exact sum even under cancellation.
+ *
+ * Errors: EP_ERR_INVALID_ARG for negative dims, NULL/misaligned pointers or
+ * overlaps.
+ */
+ep_status ep_bias_add(ep_dtype t, const void* X, const int64_t* shape,
+                      const void* bias, const void* skip, void* Y,
+                      ep_stream_t stream);
+
+/*
+ * QuickGelu
+ *   com.microsoft.QuickGelu manifest: `description`, `attributes.alpha`.
+ *
+ *   Y = X * sigmoid(alpha * X)       elementwise over numel elements
+ *
+ * alpha   the op's default is 1.702.
+ *
+ * Errors: EP_ERR_INVALID_ARG for numel < 0, NULL/misaligned pointers or
+ * overlaps.
+ */
+ep_status ep_quick_gelu(ep_dtype t, const void* X, int64_t numel, float alpha,
+                        void* Y, ep_stream_t stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* TRANSFORMER_EPILOGUE_EP_H */

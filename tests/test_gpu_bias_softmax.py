@@ -1,0 +1,179 @@
+"""BiasSoftmax: CUDA path (through the C ABI) vs the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gen import synth
+from tests._helpers import Guarded, assert_norm_close, offset_copy, to_np64
+
+pytestmark = pytest.mark.gpu
+
+
+def run(lib, data, bias, axis, inner, offsets=None, guard=True, workspace=None):
+    offsets = offsets or {}
+    keep = []
+
+    def dev(name, t):
+        if name in offsets:
+            raw, v = offset_copy(t, offsets[name])
+            keep.append(raw)
+            return v
+        return t.cuda()
+
+    g = Guarded(data.shape, data.dtype, offset_bytes=offsets.get("output", 0))
+    lib.ep_bias_softmax(dev("data", data), dev("bias", bias), axis=axis, is_inner_broadcast=inner,
+                        output=g.tensor, workspace=workspace)
+    torch.cuda.synchronize()
+    if guard:
+        g.check()
+    return g.tensor.cpu()
+
+
+def check(data, bias, axis, inner, out, rows=None):
+    o = oracle.bias_softmax(data, bias, axis=axis, is_inner_broadcast=inner, rows=rows)
+    dims = oracle.bias_softmax_dims(tuple(data.shape), bias.numel(), axis)
+    got = out.reshape(dims["batch"], dims["block"])
+    if rows is not None:
+        got = got[rows]
+    return assert_norm_close(got, o, data.dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("cols", [1, 2, 3, 7, 8, 9, 31, 32, 33, 64, 100, 255, 256, 257, 512, 513, 1000, 1024,
+                                  2047, 4096, 4100, 8192, 16384])
+def test_row_path_sizes(lib, dtype, cols):
+    rows = 24 if cols <= 4096 else 6
+    d = synth.bias_softmax_inputs((rows, cols), (3, cols), dtype, data_std=3.0, seed=cols)
+    for inner in (0, 1):
+        out = run(lib, d["data"], d["bias"], 1, inner)
+        check(d["data"], d["bias"], 1, inner, out)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("cols", [16385, 20000, 65536, 65537, 100003, 262144])
+def test_split_path_sizes(lib, dtype, cols):
+    rows = 4
+    d = synth.bias_softmax_inputs((rows, cols), (2, cols), dtype, data_std=2.0, seed=cols)
+    assert lib.ep_bias_softmax_workspace_size(d["data"].dtype, d["data"].shape, 1) > 0
+    for inner in (0, 1):
+        out = run(lib, d["data"], d["bias"], 1, inner)
+        check(d["data"], d["bias"], 1, inner, out)
+        np.testing.assert_allclose(to_np64(out).sum(axis=1), 1.0, atol=5e-3 if dtype == "f16" else 1e-4)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("axis,bias_shape,inner", [
+    (3, (2, 1, 1, 40), 1), (3, (1, 3, 4, 40), 0), (2, (2, 1, 4, 40), 1), (2, (1, 1, 4, 40), 0),
+    (1, (1, 3, 4, 40), 0), (-1, (1, 1, 1, 40), 1), (-3, (2, 3, 4, 40), 0), (0, (2, 3, 4, 40), 1),
+])
+def test_axes_and_bias_forms(lib, dtype, axis, bias_shape, inner):
+    d = synth.bias_softmax_inputs((2, 3, 4, 40), bias_shape, dtype, data_std=2.0, seed=11)
+    out = run(lib, d["data"], d["bias"], axis, inner)
+    check(d["data"], d["bias"], axis, inner, out)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16])
+@pytest.mark.parametrize("inner", [0, 1])
+@pytest.mark.parametrize("rows,cols,bias_rows", [(48, 64, 8), (48, 64, 48), (64, 512, 16), (12, 20000, 4)])
+def test_bias_row_map_bit_exact(lib, dtype, inner, rows, cols, bias_rows):
+    # data = 0; bias row k is MASKED except 0 at column k.  The output row is
+    # then exactly one-hot at its bias row's column (exp(0)=1, exp(-10000)=0).
+    data = torch.zeros(rows, cols, dtype=dtype)
+    bias = torch.full((bias_rows, cols), synth.MASKED, dtype=dtype)
+    bias[torch.arange(bias_rows), torch.arange(bias_rows)] = 0.0
+    out = run(lib, data, bias, 1, inner)
+    br = oracle.bias_row_of(np.arange(rows), bias_rows, rows // bias_rows, inner)
+    want = torch.zeros(rows, cols, dtype=dtype)
+    want[torch.arange(rows), torch.from_numpy(br)] = 1.0
+    assert torch.equal(out, want)
+
+
+def test_causal_mask_rows(lib):
+    d = synth.bias_softmax_inputs((2, 4, 64, 64), (2, 64, 64), "f16", data_std=4.0, seed=1, causal=True)
+    out = run(lib, d["data"], d["bias"], 3, 1)
+    check(d["data"], d["bias"], 3, 1, out)
+    # masked keys get exactly 0 (exp(-10000 - m) underflows)
+    o = out.reshape(-1, 64)
+    br = oracle.bias_row_of(np.arange(o.shape[0]), 128, 4, 1)  # 512 rows, 128 bias rows
+    for r in range(0, o.shape[0], 37):
+        q = br[r] % 64
+        assert (o[r, q + 1:] == 0).all()
+
+
+@pytest.mark.parametrize("dtype,offs", [("f16", {"data": 2}), ("f16", {"output": 2, "bias": 4}),
+                                        ("f32", {"data": 4, "output": 4}), ("f32", {"bias": 8})])
+@pytest.mark.parametrize("cols", [512, 30000])
+def test_misaligned_pointers(lib, dtype, offs, cols):
+    d = synth.bias_softmax_inputs((6, cols), (3, cols), dtype, data_std=2.0, seed=4)
+    out = run(lib, d["data"], d["bias"], 1, 1, offsets=offs)
+    check(d["data"], d["bias"], 1, 1, out)
+
+
+@pytest.mark.parametrize("cols", [512, 70000])
+def test_in_place(lib, cols):
+    d = synth.bias_softmax_inputs((8, cols), (2, cols), "f32", data_std=2.0, seed=8)
+    x = d["data"].cuda()
+    lib.ep_bias_softmax(x, d["bias"].cuda(), axis=1, is_inner_broadcast=0, output=x)
+    torch.cuda.synchronize()
+    check(d["data"], d["bias"], 1, 0, x.cpu())
+
+
+def test_large_equal_logits_and_neg_inf(lib):
+    data = torch.tensor([[60000.0, 60000.0, -float("inf"), 0.0]], dtype=torch.float16)
+    bias = torch.zeros(1, 4, dtype=torch.float16)
+    out = run(lib, data, bias, 1, 0)
+    assert out.tolist() == [[0.5, 0.5, 0.0, 0.0]]
+
+
+def test_all_masked_row_is_nan(lib):
+    data = torch.full((2, 40000), -float("inf"))
+    bias = torch.zeros(1, 40000)
+    out = run(lib, data, bias, 1, 0)
+    assert torch.isnan(out).all()
+    data = torch.full((2, 100), -float("inf"))
+    out = run(lib, data, torch.zeros(1, 100), 1, 0)
+    assert torch.isnan(out).all()
+
+
+def test_empty_launches_nothing(lib):
+    n0 = lib.kernel_launch_count()
+    x = torch.empty(0, 16, device="cuda")
+    b = torch.empty(0, device="cuda")
+    lib.ep_bias_softmax(x, b, axis=1, is_inner_broadcast=1)
+    assert lib.kernel_launch_count() == n0
+
+
+def test_workspace_too_small_is_rejected(lib):
+    x = torch.zeros(2, 70000, device="cuda")
+    b = torch.zeros(70000, device="cuda")
+    need = lib.ep_bias_softmax_workspace_size(torch.float32, (2, 70000), 1)
+    assert need > 0
+    ws = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(lib.EpError) as e:
+        lib.ep_bias_softmax(x, b, axis=1, is_inner_broadcast=0, workspace=ws)
+    assert e.value.status == lib.EP_ERR_WORKSPACE
+
+
+# ---------------------------------------------------------------------------
+# the measured workloads
+# ---------------------------------------------------------------------------
+
+@pytest.mark.slow
+def test_workload_attention_f16_sampled_rows(lib):
+    d = synth.workload("bias_softmax_f16_32x16x512x512_causal")
+    out = run(lib, d["data"], d["bias"], d["axis"], d["is_inner_broadcast"])
+    rows = synth.sample_rows(32 * 16 * 512, 1024)
+    check(d["data"], d["bias"], d["axis"], d["is_inner_broadcast"], out, rows=rows)
+    sums = out.reshape(-1, 512).float().sum(dim=1)
+    assert float((sums - 1).abs().max()) < 0.02
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,inner", [("bias_softmax_f32_64x262144_cyclic", 0),
+                                        ("bias_softmax_f32_8x1048576", 0),
+                                        ("bias_softmax_f32_8x1048576", 1)])
+def test_workload_long_rows_full(lib, name, inner):
+    d = synth.workload(name)
+    out = run(lib, d["data"], d["bias"], d["axis"], inner)
+    check(d["data"], d["bias"], d["axis"], inner, out)

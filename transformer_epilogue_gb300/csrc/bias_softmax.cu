@@ -1,0 +1,333 @@
+// BiasSoftmax kernels.
+//
+// Definition: com.microsoft.BiasSoftmax manifest, `description`, `derive`
+// (axisNorm, batchCount, blockSize, biasBlockCount, biasContract) and
+// `attributeDescriptions.is_inner_broadcast`: output[r] = softmax(data[r] +
+// bias[br(r)]) over blockSize columns, br(r) = r / innerRepeat (inner) or
+// r % biasBlockCount (outer).  The manifest's variants `adaptive_row` (one
+// workgroup per row) and `longrow_split` (block_stats -> row_stats ->
+// normalize, rows >= 65536) are the prior art for the two paths below.
+//
+// Row path (rows that fit on chip): a group of TPR threads owns a row; z is
+// kept in float32 registers, so data and output cross HBM once.  Max and sum
+// are warp-shuffle (+ shared memory) reductions.
+//
+// Split-row path (longer rows): the row is cut into chunks of one CTA each.
+//   k_softmax_chunk_stats   : per chunk (m_b, s_b) = (max z, sum exp(z - m_b))
+//                             -> workspace
+//   k_softmax_chunk_normalize: every CTA first combines its row's chunk stats,
+//                             M = max m_b, S = sum s_b exp(m_b - M) (the
+//                             manifest's separate row_stats pass is folded in
+//                             here), then re-reads its chunk and writes
+//                             exp(z - M) / S.
+// The host runs the pair over windows of rows sized to stay resident in L2,
+// so the second read of a chunk is normally served from L2, not HBM.
+#include <algorithm>
+#include <cmath>
+
+#include "device_common.cuh"
+#include "ep_internal.h"
+
+namespace ep {
+namespace {
+
+using dev::Frag;
+
+struct SmKernelArgs {
+  const void* data;
+  const void* bias;
+  void* output;
+  int64_t rows;
+  int64_t cols;
+  int64_t bias_rows;
+  int64_t inner_repeat;
+  bool inner;
+};
+
+__device__ __forceinline__ int64_t bias_row(const SmKernelArgs& a, int64_t r) {
+  return a.inner ? r / a.inner_repeat : r % a.bias_rows;
+}
+
+template <typename T, int VW, int TPR, int NV>
+__global__ void __launch_bounds__(TPR > 256 ? TPR : 256)
+k_bias_softmax_rows(const SmKernelArgs a) {
+  constexpr int BS = TPR > 256 ? TPR : 256;
+  constexpr int RPC = BS / TPR;
+  __shared__ float red_a[BS / 32];
+  __shared__ float red_b[BS / 32];
+  const T* data = static_cast<const T*>(a.data);  // may alias output (in place)
+  const T* __restrict__ bias = static_cast<const T*>(a.bias);
+  T* out = static_cast<T*>(a.output);
+  const int g = threadIdx.x / TPR;
+  const int lane = threadIdx.x % TPR;
+  const int64_t C = a.cols;
+
+  for (int64_t base = int64_t(blockIdx.x) * RPC; base < a.rows; base += int64_t(gridDim.x) * RPC) {
+    const int64_t r = base + g;
+    const bool active = r < a.rows;
+    Frag<T, VW> z[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+      for (int e = 0; e < VW; ++e) z[v].v[e] = -INFINITY;
+    if (active) {
+      const int64_t off = r * C;
+      const int64_t boff = bias_row(a, r) * C;
+      Frag<T, VW> b[NV];
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int64_t c = int64_t(v * TPR + lane) * VW;
+        if (c < C) {
+          z[v].load_stream(data + off + c);
+          b[v].load_keep(bias + boff + c);
+        }
+      }
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int64_t c = int64_t(v * TPR + lane) * VW;
+        if (c < C) {
+#pragma unroll
+          for (int e = 0; e < VW; ++e) z[v].v[e] = z[v].v[e] + b[v].v[e];
+        }
+      }
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+      for (int e = 0; e < VW; ++e) m = fmaxf(m, z[v].v[e]);
+    m = dev::group_max<TPR>(m, red_a);
+    float s = 0.f;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const int64_t c = int64_t(v * TPR + lane) * VW;
+#pragma unroll
+      for (int e = 0; e < VW; ++e) {
+        z[v].v[e] = (c < C) ? __expf(z[v].v[e] - m) : 0.f;
+        s += z[v].v[e];
+      }
+    }
+    s = dev::group_sum<TPR>(s, red_b);
+    const float inv = 1.0f / s;
+    if (active) {
+      const int64_t off = r * C;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int64_t c = int64_t(v * TPR + lane) * VW;
+        if (c < C) {
+#pragma unroll
+          for (int e = 0; e < VW; ++e) z[v].v[e] *= inv;
+          z[v].store_stream(out + off + c);
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// split-row path: one 256-thread CTA per chunk of kSplitThreads*NV*VW columns
+// ---------------------------------------------------------------------------
+
+constexpr int kSplitThreads = 256;
+// 32 floats of the chunk per thread for every path: 8192 columns per chunk.
+constexpr int64_t kChunk = 8192;
+template <int VW> struct SplitNV { static constexpr int value = int(kChunk / kSplitThreads / VW); };
+
+// Loads the chunk's z = data + bias (columns beyond the row are -inf).
+template <typename T, int VW, int NV = SplitNV<VW>::value>
+__device__ __forceinline__ void load_chunk(const SmKernelArgs& a, int64_t r, int64_t c0,
+                                           Frag<T, VW> (&z)[NV]) {
+  const T* data = static_cast<const T*>(a.data);
+  const T* bias = static_cast<const T*>(a.bias);
+  const int64_t off = r * a.cols;
+  const int64_t boff = bias_row(a, r) * a.cols;
+  Frag<T, VW> b[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int64_t c = c0 + int64_t(v * kSplitThreads + threadIdx.x) * VW;
+    if (c < a.cols) {
+      z[v].load_stream(data + off + c);
+      b[v].load_keep(bias + boff + c);
+    }
+  }
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int64_t c = c0 + int64_t(v * kSplitThreads + threadIdx.x) * VW;
+#pragma unroll
+    for (int e = 0; e < VW; ++e) z[v].v[e] = (c < a.cols) ? z[v].v[e] + b[v].v[e] : -INFINITY;
+  }
+}
+
+template <typename T, int VW>
+__global__ void __launch_bounds__(kSplitThreads)
+k_softmax_chunk_stats(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t nchunks, float2* stats) {
+  __shared__ float red_a[kSplitThreads / 32];
+  __shared__ float red_b[kSplitThreads / 32];
+  const int64_t total = nrows * nchunks;
+  for (int64_t blk = blockIdx.x; blk < total; blk += gridDim.x) {
+    const int64_t r = row0 + blk / nchunks;
+    const int64_t ch = blk % nchunks;
+    constexpr int NV = SplitNV<VW>::value;
+    Frag<T, VW> z[NV];
+    load_chunk<T, VW>(a, r, ch * kChunk, z);
+    float m = -INFINITY;
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+      for (int e = 0; e < VW; ++e) m = fmaxf(m, z[v].v[e]);
+    m = dev::group_max<kSplitThreads>(m, red_a);
+    float s = 0.f;
+    if (m != -INFINITY) {
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int e = 0; e < VW; ++e) s += __expf(z[v].v[e] - m);
+    }
+    s = dev::group_sum<kSplitThreads>(s, red_b);
+    if (threadIdx.x == 0) stats[r * nchunks + ch] = make_float2(m, s);
+  }
+}
+
+template <typename T, int VW>
+__global__ void __launch_bounds__(kSplitThreads)
+k_softmax_chunk_normalize(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t nchunks,
+                          const float2* stats) {
+  __shared__ float red_a[kSplitThreads / 32];
+  __shared__ float red_b[kSplitThreads / 32];
+  constexpr int NV = SplitNV<VW>::value;
+  T* out = static_cast<T*>(a.output);
+  const int64_t total = nrows * nchunks;
+  for (int64_t blk = blockIdx.x; blk < total; blk += gridDim.x) {
+    const int64_t r = row0 + blk / nchunks;
+    const int64_t ch = blk % nchunks;
+    // issue this chunk's loads first; the row combine below overlaps them
+    Frag<T, VW> z[NV];
+    load_chunk<T, VW>(a, r, ch * kChunk, z);
+    // combine the row's chunk statistics
+    const float2* st = stats + r * nchunks;
+    float M = -INFINITY;
+    for (int64_t j = threadIdx.x; j < nchunks; j += kSplitThreads) M = fmaxf(M, st[j].x);
+    M = dev::group_max<kSplitThreads>(M, red_a);
+    float S = 0.f;
+    for (int64_t j = threadIdx.x; j < nchunks; j += kSplitThreads) {
+      const float2 p = st[j];
+      if (p.x != -INFINITY) S += p.y * __expf(p.x - M);
+    }
+    S = dev::group_sum<kSplitThreads>(S, red_b);
+    const float inv = 1.0f / S;
+    const int64_t off = r * a.cols;
+    const int64_t c0 = ch * kChunk;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const int64_t c = c0 + int64_t(v * kSplitThreads + threadIdx.x) * VW;
+      if (c < a.cols) {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) z[v].v[e] = __expf(z[v].v[e] - M) * inv;
+        z[v].store_stream(out + off + c);
+      }
+    }
+    // red_a/red_b reuse by the next chunk is ordered by the two barriers of
+    // the reductions: a warp writes red_a again only after every warp has
+    // passed this chunk's second barrier, i.e. after it has read red_a.
+  }
+}
+
+// ---------------------------------------------------------------------------
+// launch planning
+// ---------------------------------------------------------------------------
+
+using RowFn = void (*)(SmKernelArgs);
+
+// Row-group shapes per (T, VW) in order of capacity; each keeps at most 32
+// floats of the row per thread.  The largest holds kRowMax columns; longer rows
+// take the split-row path.
+constexpr int64_t kRowMax = 16384;
+
+template <typename T, int VW>
+RowFn pick_row_kernel(int64_t cols, int* tpr_out) {
+  const int64_t nfrag = cols / VW;
+#define EP_SM_CASE(TPR_, NV_)                        \
+  if (nfrag <= int64_t(TPR_) * NV_) {                \
+    *tpr_out = TPR_;                                 \
+    return k_bias_softmax_rows<T, VW, TPR_, NV_>;    \
+  }
+  if constexpr (VW == 8) {
+    EP_SM_CASE(32, 1) EP_SM_CASE(32, 2) EP_SM_CASE(32, 4) EP_SM_CASE(64, 4)
+    EP_SM_CASE(128, 4) EP_SM_CASE(256, 4) EP_SM_CASE(512, 4)
+  } else if constexpr (VW == 4) {
+    EP_SM_CASE(32, 1) EP_SM_CASE(32, 2) EP_SM_CASE(32, 4) EP_SM_CASE(32, 8)
+    EP_SM_CASE(64, 8) EP_SM_CASE(128, 8) EP_SM_CASE(256, 8) EP_SM_CASE(512, 8)
+  } else {
+    EP_SM_CASE(32, 1) EP_SM_CASE(32, 2) EP_SM_CASE(32, 4) EP_SM_CASE(32, 8)
+    EP_SM_CASE(64, 8) EP_SM_CASE(128, 8) EP_SM_CASE(256, 8) EP_SM_CASE(512, 8)
+    EP_SM_CASE(512, 16) EP_SM_CASE(512, 32)
+  }
+#undef EP_SM_CASE
+  return nullptr;
+}
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <typename T>
+bool vec_ok(const void* data, const void* bias, const void* out, int64_t cols) {
+  return cols % dev::Vec16<T>::N == 0 && al16(data) && al16(bias) && al16(out);
+}
+
+template <typename T, int VW>
+cudaError_t launch_split(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_count, int l2_bytes,
+                         cudaStream_t stream, int* launches) {
+  const int64_t nchunks = (a.cols + kChunk - 1) / kChunk;
+  float2* stats = static_cast<float2*>(a.workspace);
+  // rows per window: keep a window's data within 3/4 of L2 so that the second
+  // read (normalize) hits L2
+  const int64_t row_bytes = a.cols * int64_t(sizeof(T));
+  const int64_t budget = std::max<int64_t>(int64_t(l2_bytes) * 3 / 4, 1);
+  const int64_t win = std::max<int64_t>(1, budget / row_bytes);
+  const int64_t cap = int64_t(sm_count) * 8 * 16;
+  for (int64_t r0 = 0; r0 < a.rows; r0 += win) {
+    const int64_t nr = std::min(win, a.rows - r0);
+    const unsigned grid = static_cast<unsigned>(std::min(nr * nchunks, cap));
+    k_softmax_chunk_stats<T, VW><<<grid, kSplitThreads, 0, stream>>>(k, r0, nr, nchunks, stats);
+    k_softmax_chunk_normalize<T, VW><<<grid, kSplitThreads, 0, stream>>>(k, r0, nr, nchunks, stats);
+    *launches += 2;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <typename T>
+cudaError_t launch_t(const SoftmaxArgs& a, int sm_count, int l2_bytes, cudaStream_t stream, int* launches) {
+  constexpr int VW = dev::Vec16<T>::N;
+  SmKernelArgs k{a.data, a.bias, a.output, a.rows, a.cols, a.bias_rows, a.inner_repeat, a.inner};
+  const bool vec = vec_ok<T>(a.data, a.bias, a.output, a.cols);
+  if (a.cols <= kRowMax) {
+    int tpr = 0;
+    RowFn fn = vec ? pick_row_kernel<T, VW>(a.cols, &tpr) : pick_row_kernel<T, 1>(a.cols, &tpr);
+    const int bs = std::max(tpr, 256);
+    const int rpc = bs / tpr;
+    const int64_t need = (a.rows + rpc - 1) / rpc;
+    const int64_t cap = int64_t(sm_count) * 64 * (2048 / bs);
+    fn<<<static_cast<unsigned>(std::min(need, cap)), bs, 0, stream>>>(k);
+    *launches += 1;
+    return cudaGetLastError();
+  }
+  return vec ? launch_split<T, VW>(k, a, sm_count, l2_bytes, stream, launches)
+             : launch_split<T, 1>(k, a, sm_count, l2_bytes, stream, launches);
+}
+
+}  // namespace
+
+size_t softmax_workspace_bytes(DType, int64_t rows, int64_t cols) {
+  if (rows <= 0 || cols <= kRowMax) return 0;
+  const int64_t nchunks = (cols + kChunk - 1) / kChunk;
+  return static_cast<size_t>(rows * nchunks) * sizeof(float2);
+}
+
+cudaError_t launch_bias_softmax(const SoftmaxArgs& a, int sm_count, int l2_bytes, cudaStream_t stream,
+                                int* launches) {
+  return a.t == DType::F32 ? launch_t<float>(a, sm_count, l2_bytes, stream, launches)
+                           : launch_t<__half>(a, sm_count, l2_bytes, stream, launches);
+}
+
+}  // namespace ep
