@@ -148,6 +148,37 @@ ep_status ep_bias_softmax(ep_dtype t,
 size_t ep_bias_softmax_workspace_size(ep_dtype t, const int64_t* shape, int rank, int axis);
 
 /*
+ * BiasSoftmax without a caller-provided workspace.
+ *   The op definition has no counterpart to this entry point: it is a variant
+ *   of ep_bias_softmax for callers that cannot allocate device memory, e.g. a
+ *   plugin or engine whose device memory is all reserved at start-up, code
+ *   running inside an allocator or memory-pool callback, or a loop that cannot
+ *   afford the device-wide synchronisation cudaMalloc/cudaFree may cause.  Such
+ *   callers have no way to provide the scratch the split-row path needs.
+ *
+ * Same arguments, results and errors as ep_bias_softmax, minus the workspace.
+ * The split-row scratch comes from a fixed 1 MiB device array inside the
+ * library (held by every device that loads the library until process exit),
+ * so rows * ceil(blockSize / 8192) must not exceed 131072 when blockSize >
+ * 16384; larger shapes return EP_ERR_WORKSPACE before anything is enqueued.
+ * Rows of up to 16384 elements need no scratch and have no such limit.
+ * This entry point allocates nothing.
+ *
+ * The first call on a device that needs the scratch looks up its device
+ * address (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.  All calls share the one array, which keeps
+ * the previous call's contents: every entry a call reads is written earlier in
+ * the same call, so nothing needs clearing, but calls that may overlap on the
+ * GPU (other streams, other threads) race on the array and must be ordered by
+ * the caller.
+ */
+ep_status ep_bias_softmax_noalloc(ep_dtype t,
+                                  const void* data, const int64_t* shape, int rank,
+                                  const void* bias, int64_t bias_numel,
+                                  int axis, int is_inner_broadcast,
+                                  void* output, ep_stream_t stream);
+
+/*
  * BiasAdd
  *   com.microsoft.BiasAdd manifest: `description`, `inputs`, `outputs`.
  *

@@ -40,6 +40,11 @@ def softmax(lib, t=F32, data=A, shape=(4, 8), bias=B, bias_numel=8, axis=1, inne
     return lib.ep_bias_softmax(t, data, s, r, bias, bias_numel, axis, inner, out, ws, wsb, None)
 
 
+def softmax_noalloc(lib, t=F32, data=A, shape=(4, 8), bias=B, bias_numel=8, axis=1, inner=1, out=C):
+    s, r = shp(*shape)
+    return lib.ep_bias_softmax_noalloc(t, data, s, r, bias, bias_numel, axis, inner, out, None)
+
+
 def bias_add(lib, t=F16, x=A, shape=(2, 3, 8), bias=B, skip=C, y=D):
     s, _ = shp(*shape)
     return lib.ep_bias_add(t, x, s, bias, skip, y, None)
@@ -117,6 +122,16 @@ def cases(lib):
          softmax(lib, shape=(2, 70000), bias_numel=70000, ws=D, wsb=1 << 20), CUDA),
         ("softmax long row, workspace overlaps data",
          softmax(lib, shape=(2, 70000), bias_numel=70000, ws=A, wsb=1 << 20), WORKSPACE),
+        # --- BiasSoftmax without a workspace (fixed scratch of 131072 chunk entries)
+        ("softmax noalloc one chunk beyond the fixed scratch",      # 43691 rows x 3 chunks = 131073
+         softmax_noalloc(lib, shape=(43691, 16385), bias_numel=16385), WORKSPACE),
+        ("softmax noalloc just within the fixed scratch",           # 43690 x 3 = 131070
+         softmax_noalloc(lib, shape=(43690, 16385), bias_numel=16385), CUDA),
+        ("softmax noalloc long rows within the limit", softmax_noalloc(lib, shape=(2, 70000), bias_numel=70000), CUDA),
+        ("softmax noalloc row path, any row count", softmax_noalloc(lib, shape=(1 << 22, 512), bias_numel=512), CUDA),
+        ("softmax noalloc contract", softmax_noalloc(lib, bias_numel=12), INVALID),
+        ("softmax noalloc in place ok", softmax_noalloc(lib, out=A), CUDA),
+        ("softmax noalloc empty ok", softmax_noalloc(lib, shape=(0, 8), bias_numel=0, data=None, bias=None, out=None), OK),
         # --- BiasAdd
         ("bias_add bf16 unsupported", bias_add(lib, t=BF16), UNSUPPORTED),
         ("bias_add negative dim", bias_add(lib, shape=(2, -3, 8)), INVALID),

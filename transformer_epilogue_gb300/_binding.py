@@ -44,6 +44,8 @@ _SIGNATURES = {
     "ep_bias_softmax": (ctypes.c_int, [ctypes.c_int, _vp, _i64p, ctypes.c_int, _vp, ctypes.c_int64,
                                        ctypes.c_int, ctypes.c_int, _vp, _vp, ctypes.c_size_t, _vp]),
     "ep_bias_softmax_workspace_size": (ctypes.c_size_t, [ctypes.c_int, _i64p, ctypes.c_int, ctypes.c_int]),
+    "ep_bias_softmax_noalloc": (ctypes.c_int, [ctypes.c_int, _vp, _i64p, ctypes.c_int, _vp, ctypes.c_int64,
+                                               ctypes.c_int, ctypes.c_int, _vp, _vp]),
     "ep_bias_add": (ctypes.c_int, [ctypes.c_int, _vp, _i64p, _vp, _vp, _vp, _vp]),
     "ep_quick_gelu": (ctypes.c_int, [ctypes.c_int, _vp, ctypes.c_int64, ctypes.c_float, _vp, _vp]),
 }
@@ -173,6 +175,28 @@ def ep_bias_softmax(data, bias, axis=DEFAULT_AXIS, is_inner_broadcast=None, outp
     st = lib.ep_bias_softmax(_dtype(data), _ptr(data), _shape(data.shape), data.dim(), _ptr(bias),
                              int(bias.numel()), int(axis), int(is_inner_broadcast), _ptr(output),
                              _ptr(workspace), wbytes, _stream(stream, data.device))
+    _check(st)
+    return output
+
+
+def ep_bias_softmax_noalloc(data, bias, axis=DEFAULT_AXIS, is_inner_broadcast=None, output=None, stream=None):
+    """BiasSoftmax for callers that cannot allocate device memory: the
+    split-row scratch comes from a fixed 1 MiB array inside the library
+    (rows * ceil(blockSize / 8192) <= 131072 when blockSize > 16384).  Calls
+    that may overlap on the GPU share that array and must be ordered by the
+    caller.  Pass ``output`` to keep the call free of allocations (otherwise
+    PyTorch allocates it here).  Returns output."""
+    if is_inner_broadcast is None:
+        raise ValueError("is_inner_broadcast is required")
+    lib = load_library()
+    _cuda("data", data)
+    _cuda("bias", bias)
+    if output is None:
+        output = torch.empty_like(data)
+    _cuda("output", output)
+    st = lib.ep_bias_softmax_noalloc(_dtype(data), _ptr(data), _shape(data.shape), data.dim(), _ptr(bias),
+                                     int(bias.numel()), int(axis), int(is_inner_broadcast), _ptr(output),
+                                     _stream(stream, data.device))
     _check(st)
     return output
 

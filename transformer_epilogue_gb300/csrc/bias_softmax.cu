@@ -23,6 +23,7 @@
 // The host runs the pair over windows of rows sized to stay resident in L2,
 // so the second read of a chunk is normally served from L2, not HBM.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "device_common.cuh"
@@ -328,6 +329,45 @@ cudaError_t launch_bias_softmax(const SoftmaxArgs& a, int sm_count, int l2_bytes
                                 int* launches) {
   return a.t == DType::F32 ? launch_t<float>(a, sm_count, l2_bytes, stream, launches)
                            : launch_t<__half>(a, sm_count, l2_bytes, stream, launches);
+}
+
+
+// ---------------------------------------------------------------------------
+// Fixed scratch for ep_bias_softmax_noalloc: split-row chunk statistics in a
+// file-scope device array instead of a caller-provided workspace.  Every
+// device that loads the library holds these kStaticScratchBytes until the
+// process exits.  The array's name in host code is only a stand-in, so the
+// host looks up its device address once per device (with that device current)
+// and passes that address to the kernels like any workspace.
+// ---------------------------------------------------------------------------
+
+constexpr size_t kStaticScratchBytes = size_t(1) << 20;  // 131072 (max, sum) pairs
+static __device__ __align__(256) unsigned char g_softmax_static_scratch[kStaticScratchBytes];
+
+namespace {
+constexpr int kScratchDevices = 64;
+std::atomic<void*> g_softmax_static_scratch_addr[kScratchDevices];
+}  // namespace
+
+size_t static_softmax_scratch_bytes() { return kStaticScratchBytes; }
+
+cudaError_t static_softmax_scratch(void** addr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kScratchDevices) {
+    void* p = g_softmax_static_scratch_addr[dev].load(std::memory_order_acquire);
+    if (p != nullptr) {
+      *addr = p;
+      return cudaSuccess;
+    }
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_softmax_static_scratch);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kScratchDevices) g_softmax_static_scratch_addr[dev].store(p, std::memory_order_release);
+  *addr = p;
+  return cudaSuccess;
 }
 
 }  // namespace ep

@@ -265,6 +265,53 @@ ep_status ep_bias_softmax(ep_dtype t, const void* data, const int64_t* shape, in
   return finish(e, launches, "bias_softmax");
 }
 
+ep_status ep_bias_softmax_noalloc(ep_dtype t, const void* data, const int64_t* shape, int rank, const void* bias,
+                                  int64_t bias_numel, int axis, int is_inner_broadcast, void* output,
+                                  ep_stream_t stream) {
+  SoftmaxDims d;
+  if (ep_status s = softmax_dims("bias_softmax_noalloc", t, shape, rank, axis, &d); s != EP_OK) return s;
+  if (bias_numel < 0) return fail(EP_ERR_INVALID_ARG, "bias_softmax_noalloc: negative bias_numel");
+  const int64_t bias_rows = d.block > 0 ? bias_numel / d.block : 0;
+  const bool contract = (d.numel == 0 && bias_numel == 0) ||
+                        (d.block > 0 && bias_rows > 0 && bias_numel % d.block == 0 && bias_rows <= d.batch &&
+                         d.batch % bias_rows == 0);
+  if (!contract)
+    return fail(EP_ERR_INVALID_ARG,
+                "bias_softmax_noalloc: biasContract violated (bias numel %lld, blockSize %lld, batchCount %lld)",
+                (long long)bias_numel, (long long)d.block, (long long)d.batch);
+  if (d.numel == 0) return ok();
+  if (data == nullptr || bias == nullptr || output == nullptr)
+    return fail(EP_ERR_INVALID_ARG, "bias_softmax_noalloc: data, bias and output are required");
+  const int es = esize(t);
+  if (!aligned(data, es) || !aligned(bias, es) || !aligned(output, es))
+    return fail(EP_ERR_INVALID_ARG, "bias_softmax_noalloc: pointer not aligned to the element size");
+  const Span dt{data, d.numel * es}, bs{bias, bias_numel * es}, out{output, d.numel * es};
+  if (bad_overlap_inplace_ok(out, dt) || overlap(out, bs))
+    return fail(EP_ERR_INVALID_ARG,
+                "bias_softmax_noalloc: output overlaps an input other than as an exact alias of data");
+  const size_t need = ep::softmax_workspace_bytes(to_dtype(t), d.batch, d.block);
+  const size_t cap = ep::static_softmax_scratch_bytes();
+  if (need > cap)
+    return fail(EP_ERR_WORKSPACE,
+                "bias_softmax_noalloc: this shape needs %zu bytes of split-row scratch, more than the fixed %zu "
+                "(rows * ceil(blockSize / 8192) must be <= %zu); use ep_bias_softmax with a workspace",
+                need, cap, cap / 8);
+  DevInfo dv;
+  if (ep_status s = device_info(&dv); s != EP_OK) return s;
+  void* scratch = nullptr;
+  if (need > 0) {
+    cudaError_t e = ep::static_softmax_scratch(&scratch);
+    if (e != cudaSuccess)
+      return fail(EP_ERR_CUDA, "bias_softmax_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+  }
+  ep::SoftmaxArgs a{to_dtype(t), data, bias, output, d.batch, d.block, bias_rows, d.batch / bias_rows,
+                    is_inner_broadcast != 0, scratch, need};
+  int launches = 0;
+  cudaError_t e = ep::launch_bias_softmax(a, dv.sm_count, dv.l2_bytes, reinterpret_cast<cudaStream_t>(stream),
+                                          &launches);
+  return finish(e, launches, "bias_softmax_noalloc");
+}
+
 ep_status ep_bias_add(ep_dtype t, const void* X, const int64_t* shape, const void* bias, const void* skip, void* Y,
                       ep_stream_t stream) {
   if (!valid_dtype(t)) return fail(EP_ERR_UNSUPPORTED, "bias_add: dtype %d is not float32/float16", int(t));

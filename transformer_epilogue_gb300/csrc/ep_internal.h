@@ -81,4 +81,9 @@ cudaError_t launch_quick_gelu(const QuickGeluArgs& a, int sm_count, cudaStream_t
 // on pointer alignment.
 size_t softmax_workspace_bytes(DType t, int64_t rows, int64_t cols);
 
+// Fixed device scratch of ep_bias_softmax_noalloc: its size, and its device
+// address on the current device (looked up on the first call per device).
+size_t static_softmax_scratch_bytes();
+cudaError_t static_softmax_scratch(void** addr);
+
 }  // namespace ep
