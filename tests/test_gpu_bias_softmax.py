@@ -177,3 +177,21 @@ def test_workload_long_rows_full(lib, name, inner):
     d = synth.workload(name)
     out = run(lib, d["data"], d["bias"], d["axis"], inner)
     check(d["data"], d["bias"], d["axis"], inner, out)
+
+
+# ---------------------------------------------------------------------------
+# many tiles per CTA on the shared-memory-staged row kernel, with every way a
+# tile's bias rows can be laid out (inner groups spanning tiles, outer maps
+# with all bias rows in one tile, and outer maps that wrap inside a tile)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,rows,cols,bias_rows,inner", [
+    ("f16", 80003, 512, 11429, 1), ("f16", 80003, 512, 11429, 0), ("f16", 80003, 512, 7, 0),
+    ("f16", 80003, 512, 7, 1), ("f32", 40000, 256, 40000, 0), ("f32", 30000, 1024, 3, 1),
+    ("f16", 10000, 4096, 10, 0), ("f32", 9001, 2048, 9001, 1),
+])
+def test_staged_many_tiles(lib, dtype, rows, cols, bias_rows, inner):
+    d = synth.bias_softmax_inputs((rows, cols), (bias_rows, cols), dtype, data_std=3.0, seed=rows + bias_rows)
+    out = run(lib, d["data"], d["bias"], 1, inner)
+    sample = sorted(set(synth.sample_rows(rows, 1500)) | set(range(rows - 17, rows)))
+    check(d["data"], d["bias"], 1, inner, out, rows=sample)

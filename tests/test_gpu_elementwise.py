@@ -161,3 +161,22 @@ def test_workload_quick_gelu_f16_full(lib):
     out = run_gelu(lib, d["X"], d["alpha"])
     # every element, including the 3-element tail after the 8-wide vectors
     assert_elementwise_close(out, oracle.quick_gelu(d["X"], d["alpha"]), torch.float16)
+
+
+# ---------------------------------------------------------------------------
+# many tiles per CTA on the shared-memory-staged kernels, ragged last tile and
+# a scalar tail
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,n", [("f16", (1 << 24) + 5), ("f32", (1 << 23) + 3), ("f16", 8192 * 3001 + 8)])
+def test_quick_gelu_staged_many_tiles(lib, dtype, n):
+    d = synth.quick_gelu_inputs(n, dtype, seed=n)
+    out = run_gelu(lib, d["X"], d["alpha"])
+    assert_elementwise_close(out, oracle.quick_gelu(d["X"], d["alpha"]), d["X"].dtype)
+
+
+@pytest.mark.parametrize("dtype,shape", [("f16", (8, 1000, 4096)), ("f32", (3, 777, 1000)), ("f16", (5, 999, 7000))])
+def test_bias_add_staged_many_tiles(lib, dtype, shape):
+    d = synth.bias_add_inputs(shape, dtype, seed=shape[1])
+    out = run_bias_add(lib, d)
+    assert_elementwise_close(out, oracle.bias_add(d["X"], d["bias"], d["skip"]), d["X"].dtype)

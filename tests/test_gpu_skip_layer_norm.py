@@ -211,3 +211,23 @@ def test_workload_full_size_sampled_rows(lib, name):
         rows2 = synth.sample_rows(R, 512, seed=99)
         want = oracle.skip_bias_sum(d["input"], d["skip"], d["bias"], rows=rows2)
         assert_bit_exact(s.reshape(-1, H)[rows2], want)
+
+
+# ---------------------------------------------------------------------------
+# many tiles per CTA: the shared-memory stage ring wraps many times; ragged
+# last tile; a broadcast skip whose rows wrap inside a tile
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,H,rows,skip_rows", [
+    ("f32", 1024, 20001, None), ("f16", 4096, 6003, None), ("f32", 1024, 20000, 2000),
+    ("f32", 768, 12007, 12007), ("f16", 2048, 9000, 3), ("f16", 512, 30001, 30001),
+])
+def test_staged_many_tiles(lib, dtype, H, rows, skip_rows):
+    if skip_rows is None or skip_rows == rows:
+        d = synth.sln_inputs((rows, H), None, dtype, has_beta=True, has_bias=True, seed=rows)
+    else:
+        d = synth.sln_inputs((rows // skip_rows, skip_rows, H), (1, skip_rows, H), dtype, has_beta=True,
+                             has_bias=False, seed=rows)
+    out, s = run(lib, d, residual=True)
+    sample = sorted(set(synth.sample_rows(rows, 1500)) | set(range(rows - 9, rows)))
+    check(d, out, s, rows=sample)

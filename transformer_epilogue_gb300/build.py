@@ -43,9 +43,9 @@ def _headers_mtime() -> float:
     return max(os.path.getmtime(h) for h in hs)
 
 
-def _compile(src: str, force: bool, verbose: bool, extra: list) -> str:
+def _compile(src: str, force: bool, verbose: bool, extra: list, build_dir: str = BUILD) -> str:
     path = os.path.join(CSRC, src)
-    obj = os.path.join(BUILD, src + ".o")
+    obj = os.path.join(build_dir, src + ".o")
     if not force and os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(path), _headers_mtime()):
         return obj
     cmd = [nvcc(), "-c", path, "-o", obj] + ARCH + COMMON + extra
@@ -59,22 +59,31 @@ def _compile(src: str, force: bool, verbose: bool, extra: list) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
-    os.makedirs(LIBDIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False,
+          defines: dict | None = None, out_dir: str | None = None) -> str:
+    """Build the library; returns its path.  ``defines`` (name -> value) are
+    passed as -D flags (the tuning constants of csrc/tuning.h); with
+    ``out_dir`` the objects and library go there instead of the package."""
+    build_dir = BUILD if out_dir is None else os.path.join(out_dir, "_build")
+    lib = LIB if out_dir is None else os.path.join(out_dir, os.path.basename(LIB))
+    os.makedirs(build_dir, exist_ok=True)
+    os.makedirs(os.path.dirname(lib), exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    extra += [f"-D{k}={v}" for k, v in (defines or {}).items()]
+    force = force or bool(defines)
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, force or ptxas_verbose, verbose or ptxas_verbose, extra), SOURCES))
-    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, force or ptxas_verbose, verbose or ptxas_verbose, extra, build_dir),
+                           SOURCES))
+    if force or not os.path.exists(lib) or os.path.getmtime(lib) < max(os.path.getmtime(o) for o in objs):
+        tmp = lib + ".tmp"
         cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"]
         if verbose:
             print(" ".join(cmd), flush=True)
         p = subprocess.run(cmd, capture_output=True, text=True)
         if p.returncode != 0:
             raise RuntimeError(f"link failed:\n{p.stdout}\n{p.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 def main(argv=None) -> int:

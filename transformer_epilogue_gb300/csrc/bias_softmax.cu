@@ -28,6 +28,9 @@
 
 #include "device_common.cuh"
 #include "ep_internal.h"
+#include "launch_util.h"
+#include "tma_pipe.cuh"
+#include "tuning.h"
 
 namespace ep {
 namespace {
@@ -119,6 +122,181 @@ k_bias_softmax_rows(const SmKernelArgs a) {
 #pragma unroll
           for (int e = 0; e < VW; ++e) z[v].v[e] *= inv;
           z[v].store_stream(out + off + c);
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory-staged, warp-specialised row kernel (the fast path for
+// 16-byte-aligned rows).
+//
+// A persistent CTA has kWsConsumers consumer threads in row groups of TPR and
+// one producer warp.  Tiles are RT = kWsConsumers/TPR consecutive data rows.  A
+// stage holds the tile's data rows and, after them, only the distinct bias
+// rows those data rows use (at most `bias_slots`):
+//   inner broadcast: bias rows r0/ir .. (r0+nr-1)/ir, one contiguous copy;
+//   outer, biasRows <= RT: all bias rows;
+//   outer, biasRows > RT: bias rows (r0 + j) mod biasRows, one or two copies.
+// The producer also writes each row's bias slot into the stage's header, so
+// consumers do no index division.  `full`/`empty` mbarriers per stage hand
+// stages between producer and consumers; consumer groups synchronise only
+// among themselves.
+// ---------------------------------------------------------------------------
+
+constexpr int kWsConsumers = 256;
+constexpr int kWsThreads = kWsConsumers + 32;
+constexpr int kWsConsumerWarps = kWsConsumers / 32;
+constexpr int kTmaMaxStages = 8;
+constexpr int kMaxTileRows = kWsConsumers / 16;
+
+// EXACT: the row is exactly TPR*NV fragments, so no column needs a bounds check.
+template <typename T, int TPR, int NV, bool EXACT>
+__global__ void __launch_bounds__(kWsThreads, EP_SM_TMA_MIN_CTAS)
+k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_t ntiles) {
+  constexpr int VW = dev::Vec16<T>::N;
+  constexpr int RT = kWsConsumers / TPR;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t full[kTmaMaxStages];
+  __shared__ __align__(8) uint64_t empty[kTmaMaxStages];
+  __shared__ int slot_of[kTmaMaxStages][kMaxTileRows];
+  __shared__ float red_a[kWsConsumerWarps];
+  __shared__ float red_b[kWsConsumerWarps];
+
+  const int C = static_cast<int>(a.cols);  // staged rows are at most 64 KB
+  const uint32_t row_bytes = static_cast<uint32_t>(C) * uint32_t(sizeof(T));
+  const uint32_t data_bytes = RT * row_bytes;
+  const uint32_t stage_bytes = data_bytes + uint32_t(bias_slots) * row_bytes;
+  const int tid = threadIdx.x;
+  const int64_t mine = ntiles > int64_t(blockIdx.x) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+  if (tid == 0) {
+    for (int st = 0; st < stages; ++st) {
+      dev::mbar_init(&full[st], 1);
+      dev::mbar_init(&empty[st], kWsConsumerWarps);
+    }
+    dev::mbar_init_fence();
+  }
+  __syncthreads();
+
+  if (tid >= kWsConsumers) {
+    // ---- producer ----
+    if (tid != kWsConsumers) return;
+    const T* data = static_cast<const T*>(a.data);
+    const T* bias = static_cast<const T*>(a.bias);
+    const uint64_t pol_stream = dev::policy_evict_first();
+    const uint64_t pol_keep = dev::policy_evict_last();
+    const bool outer_all = !a.inner && a.bias_rows <= RT;
+    for (int64_t j = 0; j < mine; ++j) {
+      const int st = static_cast<int>(j % stages);
+      if (j >= stages && !dev::mbar_wait(&empty[st], static_cast<uint32_t>((j / stages - 1) & 1))) {
+        for (int64_t k = j - stages; k < j; ++k)
+          dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
+        return;
+      }
+      const int64_t r0 = (blockIdx.x + j * gridDim.x) * RT;
+      const int nr = static_cast<int>(min(int64_t(RT), a.rows - r0));
+      int64_t b0 = 0, n1 = 0, n2 = 0;  // bias rows [b0, b0+n1) then [0, n2)
+      if (a.inner) {
+        b0 = r0 / a.inner_repeat;
+        n1 = (r0 + nr - 1) / a.inner_repeat - b0 + 1;
+        int64_t b = b0, left = a.inner_repeat - (r0 - b0 * a.inner_repeat);
+        for (int q = 0; q < nr; ++q) {
+          slot_of[st][q] = static_cast<int>(b - b0);
+          if (--left == 0) { ++b; left = a.inner_repeat; }
+        }
+      } else if (outer_all) {
+        n1 = a.bias_rows;
+        int64_t b = r0 % a.bias_rows;
+        for (int q = 0; q < nr; ++q) {
+          slot_of[st][q] = static_cast<int>(b);
+          if (++b == a.bias_rows) b = 0;
+        }
+      } else {
+        b0 = r0 % a.bias_rows;
+        n1 = min(int64_t(nr), a.bias_rows - b0);
+        n2 = int64_t(nr) - n1;
+        for (int q = 0; q < nr; ++q) slot_of[st][q] = q;
+      }
+      unsigned char* dst = smem + size_t(st) * stage_bytes;
+      unsigned char* bdst = dst + data_bytes;
+      // the arrive releases the slot_of writes above to the consumers
+      dev::mbar_arrive_expect_tx(&full[st], uint32_t(nr) * row_bytes + uint32_t(n1 + n2) * row_bytes);
+      dev::bulk_g2s(dst, data + r0 * C, uint32_t(nr) * row_bytes, &full[st], pol_stream);
+      dev::bulk_g2s(bdst, bias + b0 * C, uint32_t(n1) * row_bytes, &full[st], pol_keep);
+      if (n2 > 0) dev::bulk_g2s(bdst + n1 * row_bytes, bias, uint32_t(n2) * row_bytes, &full[st], pol_keep);
+    }
+    return;
+  }
+
+  // ---- consumers ----
+  T* out = static_cast<T*>(a.output);
+  const int g = tid / TPR;
+  const int lane = tid % TPR;
+  const int bar_id = 1 + g;
+  const int gwarp0 = (g * TPR) >> 5;
+
+  for (int64_t i = 0; i < mine; ++i) {
+    const int st = static_cast<int>(i % stages);
+    bool ok = dev::mbar_wait(&full[st], static_cast<uint32_t>((i / stages) & 1));
+    if constexpr (TPR > 32) ok = dev::named_barrier_and(bar_id, TPR, ok);
+    else ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return;
+
+    const int64_t r = (blockIdx.x + i * gridDim.x) * RT + g;
+    const bool active = r < a.rows;
+    const unsigned char* stage = smem + size_t(st) * stage_bytes;
+    const T* s_d = reinterpret_cast<const T*>(stage) + g * C;
+    const T* s_b = reinterpret_cast<const T*>(stage + data_bytes) + (active ? slot_of[st][g] : 0) * C;
+
+    float z[NV][VW];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const int c = (v * TPR + lane) * VW;
+      if (active && (EXACT || c < C)) {
+        float b[VW];
+        dev::lds_unpack(s_d + c, z[v]);
+        dev::lds_unpack(s_b + c, b);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) z[v][e] += b[e];
+      } else {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) z[v][e] = -INFINITY;
+      }
+    }
+    __syncwarp();
+    if ((tid & 31) == 0) dev::mbar_arrive(&empty[st]);
+
+    float m = z[0][0];
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+      for (int e = 0; e < VW; ++e) m = fmaxf(m, z[v][e]);
+    m = dev::group_max_named<TPR>(m, red_a, bar_id, gwarp0);
+    float sum = 0.f;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const int c = (v * TPR + lane) * VW;
+#pragma unroll
+      for (int e = 0; e < VW; ++e) {
+        float ev = dev::ex2_approx((z[v][e] - m) * dev::kLog2e);
+        if (!EXACT && c >= C) ev = 0.f;
+        z[v][e] = ev;
+        sum += ev;
+      }
+    }
+    sum = dev::group_sum_named<TPR>(sum, red_b, bar_id, gwarp0);
+    const float inv = 1.0f / sum;
+    if (active) {
+      T* orow = out + r * C;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int c = (v * TPR + lane) * VW;
+        if (EXACT || c < C) {
+#pragma unroll
+          for (int e = 0; e < VW; ++e) z[v][e] *= inv;
+          dev::stg_pack_stream(orow + c, z[v]);
         }
       }
     }
@@ -297,11 +475,70 @@ cudaError_t launch_split(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_cou
   return cudaSuccess;
 }
 
+using TmaRowFn = void (*)(SmKernelArgs, int, int, int64_t);
+constexpr uint32_t kTmaTileBytes = EP_SM_TMA_TILE_BYTES;
+constexpr uint32_t kTmaStageBudget = EP_SM_TMA_STAGE_BUDGET;
+
+// Same shape rule as the staged SkipLayerNorm kernel: the first TPR whose
+// NV <= 8 fragments hold the row and whose RT-row data tile is <= 16 KB.
+template <typename T>
+TmaRowFn pick_tma_row_kernel(int64_t cols, int* rows_per_tile) {
+  constexpr int VW = dev::Vec16<T>::N;
+  const int64_t nfrag = cols / VW;
+  const int64_t row_bytes = cols * int64_t(sizeof(T));
+  if (nfrag < 32) return nullptr;
+  const int tprs[] = {16, 32, 64, 128, 256};
+  for (int tpr : tprs) {
+    const int64_t nv = (nfrag + tpr - 1) / tpr;
+    if (nv > 8 || tpr < EP_SM_TMA_MIN_TPR) continue;
+    const int rt = kWsConsumers / tpr;
+    if (rt * row_bytes > kTmaTileBytes && tpr != 256) continue;
+    *rows_per_tile = rt;
+#define EP_SM_TMA_CASE(TPR_, NV_)                                                 \
+  if (tpr == TPR_ && nv <= NV_)                                                   \
+    return nfrag == int64_t(TPR_) * NV_ ? k_bias_softmax_rows_tma<T, TPR_, NV_, true> \
+                                        : k_bias_softmax_rows_tma<T, TPR_, NV_, false>;
+    EP_SM_TMA_CASE(16, 2) EP_SM_TMA_CASE(16, 4) EP_SM_TMA_CASE(32, 4) EP_SM_TMA_CASE(64, 4) EP_SM_TMA_CASE(128, 4)
+    EP_SM_TMA_CASE(256, 4) EP_SM_TMA_CASE(256, 8)
+#undef EP_SM_TMA_CASE
+    return nullptr;
+  }
+  return nullptr;
+}
+
+template <typename T>
+bool launch_tma_rows(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_count, cudaStream_t stream,
+                     int* launches, cudaError_t* err) {
+  int rt = 0;
+  TmaRowFn f = pick_tma_row_kernel<T>(a.cols, &rt);
+  if (f == nullptr) return false;
+  const uint32_t row_bytes = uint32_t(a.cols * int64_t(sizeof(T)));
+  const int64_t slots = a.inner ? std::min<int64_t>(rt, (rt - 1) / a.inner_repeat + 2)
+                                : std::min<int64_t>(rt, a.bias_rows);
+  const uint32_t stage_bytes = uint32_t(rt + slots) * row_bytes;
+  if (2 * stage_bytes > 2 * kTmaStageBudget) return false;
+  const int stages = std::min<int>(kTmaMaxStages, std::max<int>(2, kTmaStageBudget / stage_bytes));
+  const size_t smem = size_t(stages) * stage_bytes;
+  int per_sm = 1;
+  *err = resident_ctas(reinterpret_cast<const void*>(f), kWsThreads, smem, &per_sm);
+  if (*err != cudaSuccess) return true;
+  const int64_t ntiles = (a.rows + rt - 1) / rt;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(ntiles, int64_t(sm_count) * per_sm));
+  f<<<grid, kWsThreads, smem, stream>>>(k, stages, int(slots), ntiles);
+  *launches += 1;
+  *err = cudaGetLastError();
+  return true;
+}
+
 template <typename T>
 cudaError_t launch_t(const SoftmaxArgs& a, int sm_count, int l2_bytes, cudaStream_t stream, int* launches) {
   constexpr int VW = dev::Vec16<T>::N;
   SmKernelArgs k{a.data, a.bias, a.output, a.rows, a.cols, a.bias_rows, a.inner_repeat, a.inner};
   const bool vec = vec_ok<T>(a.data, a.bias, a.output, a.cols);
+  if (vec && EP_SM_TMA) {
+    cudaError_t e = cudaSuccess;
+    if (launch_tma_rows<T>(k, a, sm_count, stream, launches, &e)) return e;
+  }
   if (a.cols <= kRowMax) {
     int tpr = 0;
     RowFn fn = vec ? pick_row_kernel<T, VW>(a.cols, &tpr) : pick_row_kernel<T, 1>(a.cols, &tpr);

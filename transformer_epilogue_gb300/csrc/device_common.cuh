@@ -69,6 +69,31 @@ __device__ __forceinline__ uint4 pack(const float (&f)[8]) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// 2^x and 1/x with the hardware approximations (flush-to-zero): relative
+// errors of a few float32 ulp, used where the result is rounded to float16 or
+// must only meet an absolute tolerance.  e^x is taken as 2^(x * log2(e)).
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 16-byte shared-memory load, unpacked to float32.
+template <int VW>
+__device__ __forceinline__ void lds_unpack(const void* p, float (&f)[VW]) {
+  unpack(*reinterpret_cast<const uint4*>(p), f);
+}
+template <int VW>
+__device__ __forceinline__ void stg_pack_stream(void* p, const float (&f)[VW]) {
+  st16_stream(p, pack(f));
+}
+
 // A fragment of VW consecutive elements held as float32.  VW == Vec16<T>::N
 // uses one 128-bit access (the address must be 16-byte aligned); VW == 1 is
 // the scalar path.
@@ -85,6 +110,11 @@ template <typename T, int VW> struct Frag {
   __device__ __forceinline__ void store_stream(T* p) const {
     if constexpr (VW == 1) st1_stream(p, v[0]);
     else st16_stream(p, pack(v));
+  }
+  // 16-byte shared-memory load (VW == Vec16<T>::N only).
+  __device__ __forceinline__ void load_shared(const T* p) {
+    static_assert(VW > 1, "shared-memory fragments are 16 bytes");
+    unpack(*reinterpret_cast<const uint4*>(p), v);
   }
 };
 
@@ -135,6 +165,50 @@ __device__ __forceinline__ float group_max(float x, float* red) {
     float t = g[0];
 #pragma unroll
     for (int i = 1; i < W; ++i) t = fmaxf(t, g[i]);
+    return t;
+  }
+}
+
+// Row-group reductions that synchronise only the group: TPR <= 32 uses
+// shuffles within the warp segment; TPR > 32 (whole warps) uses a named
+// barrier `bar_id` over the group's TPR threads and the group's slots of
+// `red` (indexed by warp within the group: `gwarp0` is the group's first warp).
+template <int TPR>
+__device__ __forceinline__ float group_sum_named(float x, float* red, int bar_id, int gwarp0) {
+  if constexpr (TPR <= 32) {
+#pragma unroll
+    for (int o = TPR / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+  } else {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    constexpr int W = TPR / 32;
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) red[warp] = x;
+    asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(TPR) : "memory");
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < W; ++i) t += red[gwarp0 + i];
+    return t;
+  }
+}
+
+template <int TPR>
+__device__ __forceinline__ float group_max_named(float x, float* red, int bar_id, int gwarp0) {
+  if constexpr (TPR <= 32) {
+#pragma unroll
+    for (int o = TPR / 2; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+  } else {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    constexpr int W = TPR / 32;
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) red[warp] = x;
+    asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(TPR) : "memory");
+    float t = red[gwarp0];
+#pragma unroll
+    for (int i = 1; i < W; ++i) t = fmaxf(t, red[gwarp0 + i]);
     return t;
   }
 }

@@ -16,6 +16,9 @@
 
 #include "device_common.cuh"
 #include "ep_internal.h"
+#include "launch_util.h"
+#include "tma_pipe.cuh"
+#include "tuning.h"
 
 namespace ep {
 namespace {
@@ -145,6 +148,186 @@ k_quick_gelu(const T* x, T* y, int64_t head, int64_t nfrag, int64_t n, float alp
   }
 }
 
+// ---------------------------------------------------------------------------
+// Shared-memory-staged, warp-specialised kernels (the fast path when every
+// operand is 16-byte aligned).  A persistent CTA has kEwConsumers consumer
+// threads and one producer warp; tiles are kEwTileFrags 16-byte fragments, and
+// each of its stages holds one tile of X (and of skip, for BiasAdd), filled by
+// the producer with cp.async.bulk copies.  `full`/`empty` mbarriers per stage
+// hand stages between producer and consumers, with no CTA-wide barrier.
+// BiasAdd's bias vector is bulk-copied into shared memory once per CTA; the
+// bias column of each fragment advances incrementally (no division per
+// fragment).  Elements after the last whole fragment are done by block 0's
+// consumers with scalar loads.
+// ---------------------------------------------------------------------------
+
+constexpr int kEwConsumers = 256;
+constexpr int kEwThreads = kEwConsumers + 32;
+constexpr int kEwConsumerWarps = kEwConsumers / 32;
+constexpr int kEwTileFrags = 1024;  // 16 KB per operand per tile
+constexpr int kEwFragsPerThread = kEwTileFrags / kEwConsumers;
+constexpr int kEwMaxStages = 8;
+
+// float16 QuickGelu on the fast path: x / (1 + 2^(x * (-alpha log2 e))) with
+// the hardware 2^x and reciprocal.  u = inf gives x * 0 (NaN for x = -inf).
+__device__ __forceinline__ float quick_gelu_fast(float x, float nal2e) {
+  const float u = dev::ex2_approx(x * nal2e);
+  return x * dev::rcp_approx(1.0f + u);
+}
+
+template <typename T, bool BIAS_ADD>
+__global__ void __launch_bounds__(kEwThreads, EP_EW_TMA_MIN_CTAS)
+k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag, int64_t n, int64_t C,
+                  float alpha, int stages, uint32_t bias_bytes, uint32_t col_step_frag, uint32_t col_step_tile) {
+  constexpr int VW = dev::Vec16<T>::N;
+  constexpr int NOPS = BIAS_ADD ? 2 : 1;
+  constexpr uint32_t kTileBytes = kEwTileFrags * 16u;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t full[kEwMaxStages];
+  __shared__ __align__(8) uint64_t empty[kEwMaxStages];
+  __shared__ __align__(8) uint64_t bias_bar;
+  const int tid = threadIdx.x;
+  unsigned char* stage0 = smem + bias_bytes;  // bias_bytes is a multiple of 128
+  const uint32_t stage_bytes = NOPS * kTileBytes;
+  const int64_t ntiles = (nfrag + kEwTileFrags - 1) / kEwTileFrags;
+  const int64_t mine = ntiles > int64_t(blockIdx.x) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+  if (tid == 0) {
+    for (int st = 0; st < stages; ++st) {
+      dev::mbar_init(&full[st], 1);
+      dev::mbar_init(&empty[st], kEwConsumerWarps);
+    }
+    dev::mbar_init(&bias_bar, 1);
+    dev::mbar_init_fence();
+  }
+  __syncthreads();
+
+  if (tid >= kEwConsumers) {
+    // ---- producer ----
+    if (tid != kEwConsumers || mine == 0) return;
+    const uint64_t pol_stream = dev::policy_evict_first();
+    if constexpr (BIAS_ADD) {
+      const uint32_t cb = uint32_t(C) * uint32_t(sizeof(T));
+      dev::mbar_arrive_expect_tx(&bias_bar, cb);
+      dev::bulk_g2s(smem, bias, cb, &bias_bar, dev::policy_evict_last());
+    }
+    for (int64_t j = 0; j < mine; ++j) {
+      const int st = static_cast<int>(j % stages);
+      if (j >= stages && !dev::mbar_wait(&empty[st], static_cast<uint32_t>((j / stages - 1) & 1))) {
+        if constexpr (BIAS_ADD) dev::mbar_wait(&bias_bar, 0);
+        for (int64_t k = j - stages; k < j; ++k)
+          dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
+        return;
+      }
+      const int64_t f0 = (blockIdx.x + j * gridDim.x) * int64_t(kEwTileFrags);
+      const uint32_t bytes = static_cast<uint32_t>(min(int64_t(kEwTileFrags), nfrag - f0)) * 16u;
+      unsigned char* dst = stage0 + size_t(st) * stage_bytes;
+      dev::mbar_arrive_expect_tx(&full[st], NOPS * bytes);
+      dev::bulk_g2s(dst, x + f0 * VW, bytes, &full[st], pol_stream);
+      if constexpr (BIAS_ADD) dev::bulk_g2s(dst + kTileBytes, skip + f0 * VW, bytes, &full[st], pol_stream);
+    }
+    return;
+  }
+
+  // ---- consumers ----
+  const float nal2e = -alpha * dev::kLog2e;
+  if (blockIdx.x == 0) {  // scalar tail (elements past the last whole fragment)
+    for (int64_t e = nfrag * VW + tid; e < n; e += kEwConsumers) {
+      const float xv = dev::ld1_stream(x + e);
+      float yv;
+      if constexpr (BIAS_ADD) yv = bias_add_elem<T>(xv, dev::ld1_keep(bias + e % C), dev::ld1_stream(skip + e));
+      else yv = sizeof(T) == 4 ? quick_gelu_f32(xv, alpha) : quick_gelu_fast(xv, nal2e);
+      dev::st1_stream(y + e, yv);
+    }
+  }
+  if (mine == 0) return;
+  bool ok = true;
+  uint32_t col_tile = 0;  // bias column of this CTA's current tile's first element
+  if constexpr (BIAS_ADD) {
+    ok = dev::mbar_wait(&bias_bar, 0);
+    col_tile = static_cast<uint32_t>((int64_t(blockIdx.x) * kEwTileFrags * VW) % C);
+  }
+  const uint32_t Cu = static_cast<uint32_t>(C);
+  for (int64_t i = 0; i < mine; ++i) {
+    const int st = static_cast<int>(i % stages);
+    ok = dev::mbar_wait(&full[st], static_cast<uint32_t>((i / stages) & 1)) && ok;
+    if (!__all_sync(0xffffffffu, ok)) return;
+    const int64_t f0 = (blockIdx.x + i * gridDim.x) * int64_t(kEwTileFrags);
+    const int nf = static_cast<int>(min(int64_t(kEwTileFrags), nfrag - f0));
+    const unsigned char* src = stage0 + size_t(st) * stage_bytes;
+    float a[kEwFragsPerThread][VW];
+    float sk[BIAS_ADD ? kEwFragsPerThread : 1][VW];
+#pragma unroll
+    for (int u = 0; u < kEwFragsPerThread; ++u) {
+      const int f = u * kEwConsumers + tid;
+      if (f < nf) {
+        dev::lds_unpack(src + f * 16, a[u]);
+        if constexpr (BIAS_ADD) dev::lds_unpack(src + kTileBytes + f * 16, sk[u]);
+      }
+    }
+    __syncwarp();
+    if ((tid & 31) == 0) dev::mbar_arrive(&empty[st]);
+    uint32_t c = 0;
+    if constexpr (BIAS_ADD) {
+      c = col_tile + uint32_t(tid) * VW;
+      c = c % Cu;
+    }
+#pragma unroll
+    for (int u = 0; u < kEwFragsPerThread; ++u) {
+      const int f = u * kEwConsumers + tid;
+      if (f < nf) {
+        if constexpr (BIAS_ADD) {
+          float b[VW];
+          dev::lds_unpack(reinterpret_cast<const T*>(smem) + c, b);
+#pragma unroll
+          for (int e = 0; e < VW; ++e) a[u][e] = bias_add_elem<T>(a[u][e], b[e], sk[u][e]);
+        } else if constexpr (sizeof(T) == 4) {
+#pragma unroll
+          for (int e = 0; e < VW; ++e) a[u][e] = quick_gelu_f32(a[u][e], alpha);
+        } else {
+#pragma unroll
+          for (int e = 0; e < VW; ++e) a[u][e] = quick_gelu_fast(a[u][e], nal2e);
+        }
+        dev::stg_pack_stream(y + (f0 + f) * VW, a[u]);
+      }
+      if constexpr (BIAS_ADD) {
+        c += col_step_frag;
+        if (c >= Cu) c -= Cu;
+      }
+    }
+    if constexpr (BIAS_ADD) {
+      col_tile += col_step_tile;
+      if (col_tile >= Cu) col_tile -= Cu;
+    }
+  }
+}
+
+constexpr uint32_t kEwStageBudget = EP_EW_TMA_STAGE_BUDGET;
+constexpr int64_t kEwMaxBiasBytes = 64 * 1024;
+
+template <typename T, bool BIAS_ADD>
+cudaError_t launch_ew_tma(const T* x, const T* skip, const T* bias, T* y, int64_t n, int64_t C, float alpha,
+                          int sm_count, cudaStream_t stream) {
+  constexpr int VW = dev::Vec16<T>::N;
+  auto fn = k_elementwise_tma<T, BIAS_ADD>;
+  const int64_t nfrag = n / VW;
+  const uint32_t bias_bytes = BIAS_ADD ? uint32_t((C * int64_t(sizeof(T)) + 127) / 128 * 128) : 0u;
+  const uint32_t stage_bytes = (BIAS_ADD ? 2u : 1u) * kEwTileFrags * 16u;
+  const int stages = std::min<int>(kEwMaxStages, std::max<int>(2, kEwStageBudget / stage_bytes));
+  const size_t smem = bias_bytes + size_t(stages) * stage_bytes;
+  int per_sm = 1;
+  cudaError_t e = resident_ctas(reinterpret_cast<const void*>(fn), kEwThreads, smem, &per_sm);
+  if (e != cudaSuccess) return e;
+  const int64_t ntiles = (nfrag + kEwTileFrags - 1) / kEwTileFrags;
+  const unsigned grid =
+      static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(ntiles, int64_t(sm_count) * per_sm)));
+  const uint32_t step_frag = BIAS_ADD ? uint32_t((int64_t(kEwConsumers) * VW) % C) : 0u;
+  const uint32_t step_tile = BIAS_ADD ? uint32_t((int64_t(grid) * kEwTileFrags * VW) % C) : 0u;
+  fn<<<grid, kEwThreads, smem, stream>>>(x, skip, bias, y, nfrag, n, C, alpha, stages, bias_bytes, step_frag,
+                                         step_tile);
+  return cudaGetLastError();
+}
+
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline unsigned grid_for(int64_t work_items, int sm_count) {
@@ -160,6 +343,11 @@ cudaError_t bias_add_t(const BiasAddArgs& a, int sm_count, cudaStream_t stream, 
   const T* b = static_cast<const T*>(a.bias);
   const T* s = static_cast<const T*>(a.skip);
   T* y = static_cast<T*>(a.y);
+  if (EP_EW_TMA && a.C % VW == 0 && al16(x) && al16(b) && al16(s) && al16(y) &&
+      a.C * int64_t(sizeof(T)) <= kEwMaxBiasBytes && a.n / VW >= kEwTileFrags) {
+    *launches += 1;
+    return launch_ew_tma<T, true>(x, s, b, y, a.n, a.C, 0.f, sm_count, stream);
+  }
   if (a.C % VW == 0 && al16(x) && al16(b) && al16(s) && al16(y)) {
     const int64_t nfrag = a.n / VW;
     k_bias_add<T, VW><<<grid_for(nfrag, sm_count), kThreads, 0, stream>>>(x, b, s, y, nfrag, a.C);
@@ -177,6 +365,10 @@ cudaError_t quick_gelu_t(const QuickGeluArgs& a, int sm_count, cudaStream_t stre
   T* y = static_cast<T*>(a.y);
   const uintptr_t ox = reinterpret_cast<uintptr_t>(x) & 15u;
   const uintptr_t oy = reinterpret_cast<uintptr_t>(y) & 15u;
+  if (EP_EW_TMA && ox == 0 && oy == 0 && a.n / VW >= kEwTileFrags) {
+    *launches += 1;
+    return launch_ew_tma<T, false>(x, nullptr, nullptr, y, a.n, 1, a.alpha, sm_count, stream);
+  }
   if (ox == oy) {
     const int64_t head = std::min<int64_t>(a.n, int64_t((16 - ox) & 15u) / int64_t(sizeof(T)));
     const int64_t nfrag = (a.n - head) / VW;

@@ -19,6 +19,9 @@
 
 #include "device_common.cuh"
 #include "ep_internal.h"
+#include "launch_util.h"
+#include "tma_pipe.cuh"
+#include "tuning.h"
 
 namespace ep {
 namespace {
@@ -211,6 +214,210 @@ __global__ void __launch_bounds__(1024) k_skip_layer_norm_long(const SlnKernelAr
 }
 
 // ---------------------------------------------------------------------------
+// Shared-memory-staged, warp-specialised kernel (the fast path for 16-byte-
+// aligned rows).
+//
+// A persistent CTA has kWsConsumers consumer threads in row groups of TPR and
+// one producer warp.  Tiles are RT = kWsConsumers/TPR consecutive rows; each of
+// the `stages` shared-memory stages holds one tile: the RT input rows, then the
+// RT skip rows (for a broadcast skip, rows r mod skipRows).  Per stage, `full`
+// completes when the producer's cp.async.bulk copies have landed and `empty`
+// when all consumer warps are done with it.  The producer refills a stage as
+// soon as it is empty, so up to `stages` tiles are in flight per CTA; consumer
+// groups synchronise only among themselves (shuffles, or a named barrier when a
+// row spans several warps), never CTA-wide.  The arithmetic is that of
+// k_skip_layer_norm, reading rows from shared memory.
+// ---------------------------------------------------------------------------
+
+constexpr int kWsConsumers = 256;
+constexpr int kWsThreads = kWsConsumers + 32;
+constexpr int kWsConsumerWarps = kWsConsumers / 32;
+constexpr int kTmaMaxStages = 8;
+
+// Dynamic shared memory: [gamma | beta | bias] (each `param_stride` bytes,
+// beta/bias only when present), then the stages.  EXACT: the row is exactly
+// TPR*NV fragments, so no column needs a bounds check.
+template <typename T, int TPR, int NV, bool EXACT>
+__global__ void __launch_bounds__(kWsThreads, EP_SLN_TMA_MIN_CTAS)
+k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_t param_stride) {
+  constexpr int VW = dev::Vec16<T>::N;
+  constexpr int RT = kWsConsumers / TPR;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t full[kTmaMaxStages];
+  __shared__ __align__(8) uint64_t empty[kTmaMaxStages];
+  __shared__ __align__(8) uint64_t params_bar;
+  __shared__ float red_a[kWsConsumerWarps];
+  __shared__ float red_b[kWsConsumerWarps];
+
+  const int H = static_cast<int>(a.H);  // staged rows are at most 64 KB
+  const uint32_t row_bytes = static_cast<uint32_t>(H) * uint32_t(sizeof(T));
+  const uint32_t tile_bytes = RT * row_bytes;
+  const uint32_t stage_bytes = 2 * tile_bytes;
+  const bool has_beta = a.beta != nullptr;
+  const bool has_bias = a.bias != nullptr;
+  const uint32_t param_bytes = param_stride * (1u + has_beta + has_bias);
+  unsigned char* stage0 = smem + param_bytes;
+  const int tid = threadIdx.x;
+  const int64_t mine = ntiles > int64_t(blockIdx.x) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+  if (tid == 0) {
+    for (int st = 0; st < stages; ++st) {
+      dev::mbar_init(&full[st], 1);
+      dev::mbar_init(&empty[st], kWsConsumerWarps);
+    }
+    dev::mbar_init(&params_bar, 1);
+    dev::mbar_init_fence();
+  }
+  __syncthreads();
+  if (mine == 0) return;
+
+  if (tid >= kWsConsumers) {
+    // ---- producer: one thread issues every copy of this CTA ----
+    if (tid != kWsConsumers) return;
+    const T* in = static_cast<const T*>(a.input);
+    const T* sk = static_cast<const T*>(a.skip);
+    const uint64_t pol_stream = dev::policy_evict_first();
+    const uint64_t pol_keep = dev::policy_evict_last();
+    dev::mbar_arrive_expect_tx(&params_bar, param_bytes / param_stride * row_bytes);
+    dev::bulk_g2s(smem, a.gamma, row_bytes, &params_bar, pol_keep);
+    if (has_beta) dev::bulk_g2s(smem + param_stride, a.beta, row_bytes, &params_bar, pol_keep);
+    if (has_bias) dev::bulk_g2s(smem + param_stride * (1u + has_beta), a.bias, row_bytes, &params_bar, pol_keep);
+    for (int64_t j = 0; j < mine; ++j) {
+      const int st = static_cast<int>(j % stages);
+      if (j >= stages && !dev::mbar_wait(&empty[st], static_cast<uint32_t>((j / stages - 1) & 1))) {
+        // consumers stopped: wait (bounded) for the copies still in flight, then stop
+        dev::mbar_wait(&params_bar, 0);
+        for (int64_t k = j - stages; k < j; ++k)
+          dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
+        return;
+      }
+      const int64_t r0 = (blockIdx.x + j * gridDim.x) * RT;
+      const uint32_t nr = static_cast<uint32_t>(min(int64_t(RT), a.rows - r0));
+      unsigned char* dst = stage0 + size_t(st) * stage_bytes;
+      dev::mbar_arrive_expect_tx(&full[st], 2u * nr * row_bytes);
+      dev::bulk_g2s(dst, in + r0 * H, nr * row_bytes, &full[st], pol_stream);
+      if (!a.skip_bcast) {
+        dev::bulk_g2s(dst + tile_bytes, sk + r0 * H, nr * row_bytes, &full[st], pol_stream);
+      } else {
+        int64_t sr = r0 % a.skip_rows;
+        for (uint32_t q = 0; q < nr; ++q) {
+          dev::bulk_g2s(dst + tile_bytes + q * row_bytes, sk + sr * H, row_bytes, &full[st], pol_keep);
+          if (++sr == a.skip_rows) sr = 0;
+        }
+      }
+    }
+    return;
+  }
+
+  // ---- consumers ----
+  T* out = static_cast<T*>(a.output);
+  T* sum_out = static_cast<T*>(a.sum_out);
+  const T* p_gamma = reinterpret_cast<const T*>(smem);
+  const T* p_beta = reinterpret_cast<const T*>(smem + param_stride);
+  const T* p_bias = reinterpret_cast<const T*>(smem + param_stride * (1u + has_beta));
+  const int g = tid / TPR;
+  const int lane = tid % TPR;
+  const int bar_id = 1 + g;            // named barrier of a multi-warp group
+  const int gwarp0 = (g * TPR) >> 5;   // the group's first warp
+  bool ok = dev::mbar_wait(&params_bar, 0);
+
+  for (int64_t i = 0; i < mine; ++i) {
+    const int st = static_cast<int>(i % stages);
+    ok = dev::mbar_wait(&full[st], static_cast<uint32_t>((i / stages) & 1)) && ok;
+    if constexpr (TPR > 32) ok = dev::named_barrier_and(bar_id, TPR, ok);
+    else ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return;
+
+    const int64_t r = (blockIdx.x + i * gridDim.x) * RT + g;
+    const bool active = r < a.rows;
+    const unsigned char* stage = stage0 + size_t(st) * stage_bytes;
+    const T* s_in = reinterpret_cast<const T*>(stage) + g * H;
+    const T* s_sk = reinterpret_cast<const T*>(stage + tile_bytes) + g * H;
+
+    float s[NV][VW];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const int c = (v * TPR + lane) * VW;
+      if (active && (EXACT || c < H)) {
+        float k[VW];
+        dev::lds_unpack(s_in + c, s[v]);
+        dev::lds_unpack(s_sk + c, k);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) s[v][e] = __fadd_rn(s[v][e], k[e]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) s[v][e] = 0.f;
+      }
+    }
+    __syncwarp();
+    if ((tid & 31) == 0) dev::mbar_arrive(&empty[st]);
+
+    const int64_t off = r * H;
+    if (active && (has_bias || sum_out != nullptr)) {
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int c = (v * TPR + lane) * VW;
+        if (EXACT || c < H) {
+          if (has_bias) {
+            float b[VW];
+            dev::lds_unpack(p_bias + c, b);
+#pragma unroll
+            for (int e = 0; e < VW; ++e) s[v][e] = __fadd_rn(s[v][e], b[e]);
+          }
+          if (sum_out != nullptr) dev::stg_pack_stream(sum_out + off + c, s[v]);
+        }
+      }
+    }
+    float mean = 0.f;
+    if (!a.simplified) {
+      float t = 0.f;
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int e = 0; e < VW; ++e) t += s[v][e];
+      mean = dev::group_sum_named<TPR>(t, red_a, bar_id, gwarp0) / static_cast<float>(H);
+    }
+    // s becomes s - mean from here on
+    float q = 0.f;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const int c = (v * TPR + lane) * VW;
+#pragma unroll
+      for (int e = 0; e < VW; ++e) {
+        s[v][e] -= mean;
+        if (EXACT || c < H) q = fmaf(s[v][e], s[v][e], q);
+      }
+    }
+    const float var = dev::group_sum_named<TPR>(q, red_b, bar_id, gwarp0) / static_cast<float>(H);
+    const float rstd = 1.0f / sqrtf(var + a.eps);
+    if (active) {
+      if (lane == 0) {
+        if (a.mean_out != nullptr) a.mean_out[r] = mean;
+        if (a.inv_std_out != nullptr) a.inv_std_out[r] = rstd;
+      }
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int c = (v * TPR + lane) * VW;
+        if (EXACT || c < H) {
+          float gm[VW], y[VW];
+          dev::lds_unpack(p_gamma + c, gm);
+          if (has_beta) {
+            float bt[VW];
+            dev::lds_unpack(p_beta + c, bt);
+#pragma unroll
+            for (int e = 0; e < VW; ++e) y[e] = fmaf(s[v][e] * rstd, gm[e], bt[e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < VW; ++e) y[e] = (s[v][e] * rstd) * gm[e];
+          }
+          dev::stg_pack_stream(out + off + c, y);
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // launch planning
 // ---------------------------------------------------------------------------
 
@@ -246,6 +453,39 @@ KernelFn pick_kernel(int64_t H, int* tpr_out) {
   return nullptr;
 }
 
+// Row shapes of the staged kernel: the first threads-per-row TPR (in this
+// order) whose NV <= 8 fragments per thread hold the row and whose tile of
+// RT = 256/TPR rows is at most kTmaTileBytes (TPR = 256 takes any tile).
+constexpr uint32_t kTmaTileBytes = EP_SLN_TMA_TILE_BYTES;
+constexpr uint32_t kTmaStageBudget = EP_SLN_TMA_STAGE_BUDGET;  // shared memory for the stages of one CTA
+
+using TmaFn = void (*)(SlnKernelArgs, int, int64_t, uint32_t);
+
+template <typename T>
+TmaFn pick_tma_kernel(int64_t H, int* rows_per_tile) {
+  constexpr int VW = dev::Vec16<T>::N;
+  const int64_t nfrag = H / VW;
+  const int64_t row_bytes = H * int64_t(sizeof(T));
+  if (nfrag < 32) return nullptr;
+  const int tprs[] = {16, 32, 64, 128, 256};
+  for (int tpr : tprs) {
+    const int64_t nv = (nfrag + tpr - 1) / tpr;
+    if (nv > 8) continue;
+    const int rt = kWsConsumers / tpr;
+    if (rt * row_bytes > kTmaTileBytes && tpr != 256) continue;
+    *rows_per_tile = rt;
+#define EP_SLN_TMA_CASE(TPR_, NV_)                                                \
+  if (tpr == TPR_ && nv <= NV_)                                                  \
+    return nfrag == int64_t(TPR_) * NV_ ? k_skip_layer_norm_tma<T, TPR_, NV_, true> \
+                                        : k_skip_layer_norm_tma<T, TPR_, NV_, false>;
+    EP_SLN_TMA_CASE(16, 2) EP_SLN_TMA_CASE(16, 4) EP_SLN_TMA_CASE(32, 4) EP_SLN_TMA_CASE(64, 4) EP_SLN_TMA_CASE(128, 4)
+    EP_SLN_TMA_CASE(256, 4) EP_SLN_TMA_CASE(256, 8)
+#undef EP_SLN_TMA_CASE
+    return nullptr;
+  }
+  return nullptr;
+}
+
 template <typename T>
 cudaError_t launch_t(const SlnArgs& a, int sm_count, cudaStream_t stream, int* launches) {
   SlnKernelArgs k{a.input, a.skip, a.gamma, a.beta, a.bias, a.output, a.sum_out,
@@ -255,6 +495,27 @@ cudaError_t launch_t(const SlnArgs& a, int sm_count, cudaStream_t stream, int* l
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   const bool vec = (a.H % VW == 0) && al16(a.input) && al16(a.skip) && al16(a.gamma) &&
                    al16(a.beta) && al16(a.bias) && al16(a.output) && al16(a.sum_out);
+  if (vec && EP_SLN_TMA) {
+    int rt = 0;
+    if (TmaFn f = pick_tma_kernel<T>(a.H, &rt)) {
+      const uint32_t row_bytes = uint32_t(a.H * int64_t(sizeof(T)));
+      const uint32_t stage_bytes = 2u * uint32_t(rt) * row_bytes;
+      const uint32_t param_stride = (row_bytes + 127u) / 128u * 128u;
+      const uint32_t param_bytes = param_stride * (1u + (a.beta != nullptr) + (a.bias != nullptr));
+      const int stages = std::min<int>(kTmaMaxStages, std::max<int>(2, kTmaStageBudget / stage_bytes));
+      if (2 * stage_bytes <= 2 * kTmaStageBudget && param_bytes <= 96u * 1024u) {
+        const size_t smem = param_bytes + size_t(stages) * stage_bytes;
+        int per_sm = 1;
+        cudaError_t e = resident_ctas(reinterpret_cast<const void*>(f), kWsThreads, smem, &per_sm);
+        if (e != cudaSuccess) return e;
+        const int64_t ntiles = (a.rows + rt - 1) / rt;
+        const unsigned grid = static_cast<unsigned>(std::min<int64_t>(ntiles, int64_t(sm_count) * per_sm));
+        f<<<grid, kWsThreads, smem, stream>>>(k, stages, ntiles, param_stride);
+        *launches += 1;
+        return cudaGetLastError();
+      }
+    }
+  }
   int tpr = 0;
   KernelFn fn = vec ? pick_kernel<T, VW>(a.H, &tpr) : pick_kernel<T, 1>(a.H, &tpr);
   if (fn != nullptr) {

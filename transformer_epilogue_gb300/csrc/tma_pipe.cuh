@@ -1,0 +1,149 @@
+// Bulk-copy (TMA) staging primitives for the streaming kernels on sm_100+:
+// cp.async.bulk global->shared copies that complete on an mbarrier, and a
+// bounded wait on that barrier.
+//
+// Pipeline shape used by the kernels: a CTA owns S shared-memory stages and
+// one mbarrier per stage.  Thread 0 arms a stage's barrier with the bytes it
+// expects (arrive.expect_tx) and issues the bulk copies for a tile; all threads
+// wait for the barrier's phase, compute from shared memory, and pass a
+// __syncthreads() before thread 0 refills the stage with the tile S ahead.  The
+// copy engine keeps up to S tiles per CTA in flight without holding registers.
+//
+// Every wait is bounded (kWaitTimeoutNs of %globaltimer): a wait that runs out
+// counts itself in g_pipe_timeouts (one counter per translation unit), and the
+// kernel then waits, again bounded, for its other copies in flight before it
+// returns, so no copy can land in shared memory the CTA no longer owns.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace ep {
+namespace dev {
+
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s
+
+static __device__ unsigned int g_pipe_timeouts;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Makes the initialised barriers visible to the copy engine; follow with __syncthreads().
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_addr(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Waits until the barrier's phase with the given parity has completed, for at
+// most kWaitTimeoutNs.  Returns false (and counts a timeout) if it ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      atomicAdd(&g_pipe_timeouts, 1u);
+      return false;
+    }
+  }
+}
+
+// Plain arrive (release semantics: this thread's earlier shared-memory reads
+// are ordered before the phase completes).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
+      : "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32) with id 1..15; returns
+// true on every participating thread iff `pred` held on all of them.
+__device__ __forceinline__ bool named_barrier_and(int id, int count, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"(uint32_t(pred)), "r"(id), "r"(count)
+      : "memory");
+  return out != 0;
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Evict-first L2 policy for data that is read once.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// global to this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+      ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// 16-byte shared-memory load.
+__device__ __forceinline__ uint4 lds16(const void* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+}  // namespace dev
+
+// Host side: read and clear this translation unit's timeout counter.
+static inline cudaError_t read_and_clear_pipe_timeouts(unsigned int* count) {
+  cudaError_t e = cudaMemcpyFromSymbol(count, dev::g_pipe_timeouts, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(dev::g_pipe_timeouts, &zero, sizeof(unsigned int));
+}
+
+}  // namespace ep
