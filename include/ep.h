@@ -159,8 +159,9 @@ size_t ep_bias_softmax_workspace_size(ep_dtype t, const int64_t* shape, int rank
  * Same arguments, results and errors as ep_bias_softmax, minus the workspace.
  * The split-row scratch comes from a fixed 1 MiB device array inside the
  * library (held by every device that loads the library until process exit),
- * so rows * ceil(blockSize / 8192) must not exceed 131072 when blockSize >
- * 16384; larger shapes return EP_ERR_WORKSPACE before anything is enqueued.
+ * so rows * ceil(blockSize / chunk) must not exceed 131072 when blockSize >
+ * 16384, with chunk = 4096 for float32 and 8192 for float16; larger shapes
+ * return EP_ERR_WORKSPACE before anything is enqueued.
  * Rows of up to 16384 elements need no scratch and have no such limit.
  * This entry point allocates nothing.
  *

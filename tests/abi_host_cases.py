@@ -123,10 +123,14 @@ def cases(lib):
         ("softmax long row, workspace overlaps data",
          softmax(lib, shape=(2, 70000), bias_numel=70000, ws=A, wsb=1 << 20), WORKSPACE),
         # --- BiasSoftmax without a workspace (fixed scratch of 131072 chunk entries)
-        ("softmax noalloc one chunk beyond the fixed scratch",      # 43691 rows x 3 chunks = 131073
-         softmax_noalloc(lib, shape=(43691, 16385), bias_numel=16385), WORKSPACE),
-        ("softmax noalloc just within the fixed scratch",           # 43690 x 3 = 131070
-         softmax_noalloc(lib, shape=(43690, 16385), bias_numel=16385), CUDA),
+        ("softmax noalloc one chunk beyond the fixed scratch",      # f32: 26215 rows x 5 chunks = 131075
+         softmax_noalloc(lib, shape=(26215, 16385), bias_numel=16385), WORKSPACE),
+        ("softmax noalloc just within the fixed scratch",           # 26214 x 5 = 131070
+         softmax_noalloc(lib, shape=(26214, 16385), bias_numel=16385), CUDA),
+        ("softmax noalloc f16 within the fixed scratch",            # f16: 43690 rows x 3 chunks
+         softmax_noalloc(lib, t=F16, shape=(43690, 16385), bias_numel=16385), CUDA),
+        ("softmax noalloc f16 beyond the fixed scratch",            # 43691 x 3 = 131073
+         softmax_noalloc(lib, t=F16, shape=(43691, 16385), bias_numel=16385), WORKSPACE),
         ("softmax noalloc long rows within the limit", softmax_noalloc(lib, shape=(2, 70000), bias_numel=70000), CUDA),
         ("softmax noalloc row path, any row count", softmax_noalloc(lib, shape=(1 << 22, 512), bias_numel=512), CUDA),
         ("softmax noalloc contract", softmax_noalloc(lib, bias_numel=12), INVALID),
@@ -169,8 +173,10 @@ def main():
     # workspace size queries are pure host arithmetic
     s, r = shp(2, 70000)
     ws = lib.ep_bias_softmax_workspace_size(F32, s, r, 1)
-    if ws != 2 * 9 * 8:          # ceil(70000 / 8192) = 9 chunks of (max, sum) floats per row
-        bad.append(("workspace size (2, 70000)", ws, 144, ""))
+    if ws != 2 * 18 * 8:         # f32: ceil(70000 / 4096) = 18 chunks of (max, sum) floats per row
+        bad.append(("workspace size (2, 70000)", ws, 288, ""))
+    if lib.ep_bias_softmax_workspace_size(F16, s, r, 1) != 2 * 9 * 8:   # f16: 8192-column chunks
+        bad.append(("workspace size f16 (2, 70000)", lib.ep_bias_softmax_workspace_size(F16, s, r, 1), 144, ""))
     s, r = shp(262144, 512)
     if lib.ep_bias_softmax_workspace_size(F16, s, r, 1) != 0:
         bad.append(("workspace size of a row-path shape", 1, 0, ""))

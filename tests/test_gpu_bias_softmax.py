@@ -195,3 +195,16 @@ def test_staged_many_tiles(lib, dtype, rows, cols, bias_rows, inner):
     out = run(lib, d["data"], d["bias"], 1, inner)
     sample = sorted(set(synth.sample_rows(rows, 1500)) | set(range(rows - 17, rows)))
     check(d["data"], d["bias"], 1, inner, out, rows=sample)
+
+
+@pytest.mark.parametrize("dtype,rows,cols,bias_rows,inner", [
+    ("f32", 160, 262144, 4, 1), ("f32", 160, 262144, 4, 0), ("f16", 96, 600000, 3, 0), ("f32", 5, 16388, 5, 1),
+])
+def test_split_path_several_windows(lib, dtype, rows, cols, bias_rows, inner):
+    # more rows than one L2-sized window holds: the stats/normalize pair runs per
+    # window; chunk statistics of every row must land in the right place
+    d = synth.bias_softmax_inputs((rows, cols), (bias_rows, cols), dtype, data_std=2.0, seed=rows)
+    out = run(lib, d["data"], d["bias"], 1, inner)
+    sample = sorted(set(synth.sample_rows(rows, 12)) | {rows - 1})
+    check(d["data"], d["bias"], 1, inner, out, rows=sample)
+    np.testing.assert_allclose(to_np64(out).sum(axis=1), 1.0, atol=5e-3 if dtype == "f16" else 1e-4)

@@ -304,16 +304,22 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
 }
 
 // ---------------------------------------------------------------------------
-// split-row path: one 256-thread CTA per chunk of kSplitThreads*NV*VW columns
+// split-row path.  A row is cut into chunks of kChunkBytes (4096 float32 or
+// 8192 float16 columns); pass 1 writes each chunk's (max z, sum exp(z - max))
+// to the workspace, pass 2 combines a row's chunk statistics into
+// M = max m_b, S = sum s_b exp(m_b - M) and writes exp(z - M) / S.
 // ---------------------------------------------------------------------------
 
 constexpr int kSplitThreads = 256;
-// 32 floats of the chunk per thread for every path: 8192 columns per chunk.
-constexpr int64_t kChunk = 8192;
-template <int VW> struct SplitNV { static constexpr int value = int(kChunk / kSplitThreads / VW); };
+constexpr int64_t kChunkBytes = 16384;
+template <typename T> constexpr int64_t chunk_cols() { return kChunkBytes / int64_t(sizeof(T)); }
+template <typename T, int VW> struct SplitNV {
+  static constexpr int value = int(chunk_cols<T>() / kSplitThreads / VW);
+};
 
+// Register path (any alignment): one 256-thread CTA per chunk.
 // Loads the chunk's z = data + bias (columns beyond the row are -inf).
-template <typename T, int VW, int NV = SplitNV<VW>::value>
+template <typename T, int VW, int NV = SplitNV<T, VW>::value>
 __device__ __forceinline__ void load_chunk(const SmKernelArgs& a, int64_t r, int64_t c0,
                                            Frag<T, VW> (&z)[NV]) {
   const T* data = static_cast<const T*>(a.data);
@@ -346,9 +352,9 @@ k_softmax_chunk_stats(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t
   for (int64_t blk = blockIdx.x; blk < total; blk += gridDim.x) {
     const int64_t r = row0 + blk / nchunks;
     const int64_t ch = blk % nchunks;
-    constexpr int NV = SplitNV<VW>::value;
+    constexpr int NV = SplitNV<T, VW>::value;
     Frag<T, VW> z[NV];
-    load_chunk<T, VW>(a, r, ch * kChunk, z);
+    load_chunk<T, VW>(a, r, ch * chunk_cols<T>(), z);
     float m = -INFINITY;
 #pragma unroll
     for (int v = 0; v < NV; ++v)
@@ -373,7 +379,7 @@ k_softmax_chunk_normalize(const SmKernelArgs a, int64_t row0, int64_t nrows, int
                           const float2* stats) {
   __shared__ float red_a[kSplitThreads / 32];
   __shared__ float red_b[kSplitThreads / 32];
-  constexpr int NV = SplitNV<VW>::value;
+  constexpr int NV = SplitNV<T, VW>::value;
   T* out = static_cast<T*>(a.output);
   const int64_t total = nrows * nchunks;
   for (int64_t blk = blockIdx.x; blk < total; blk += gridDim.x) {
@@ -381,8 +387,7 @@ k_softmax_chunk_normalize(const SmKernelArgs a, int64_t row0, int64_t nrows, int
     const int64_t ch = blk % nchunks;
     // issue this chunk's loads first; the row combine below overlaps them
     Frag<T, VW> z[NV];
-    load_chunk<T, VW>(a, r, ch * kChunk, z);
-    // combine the row's chunk statistics
+    load_chunk<T, VW>(a, r, ch * chunk_cols<T>(), z);
     const float2* st = stats + r * nchunks;
     float M = -INFINITY;
     for (int64_t j = threadIdx.x; j < nchunks; j += kSplitThreads) M = fmaxf(M, st[j].x);
@@ -395,7 +400,7 @@ k_softmax_chunk_normalize(const SmKernelArgs a, int64_t row0, int64_t nrows, int
     S = dev::group_sum<kSplitThreads>(S, red_b);
     const float inv = 1.0f / S;
     const int64_t off = r * a.cols;
-    const int64_t c0 = ch * kChunk;
+    const int64_t c0 = ch * chunk_cols<T>();
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
       const int64_t c = c0 + int64_t(v * kSplitThreads + threadIdx.x) * VW;
@@ -405,9 +410,195 @@ k_softmax_chunk_normalize(const SmKernelArgs a, int64_t row0, int64_t nrows, int
         z[v].store_stream(out + off + c);
       }
     }
-    // red_a/red_b reuse by the next chunk is ordered by the two barriers of
-    // the reductions: a warp writes red_a again only after every warp has
-    // passed this chunk's second barrier, i.e. after it has read red_a.
+  }
+}
+
+// Staged path (16-byte-aligned rows): warp-specialised, persistent, each CTA
+// owning a contiguous range of the window's chunks (so it meets few rows).  A
+// stage holds one chunk of data and the matching chunk of its bias row.  Each
+// of the 8 consumer warps reduces a 1/8 slice of the chunk; pass 1 combines the
+// slices (one named barrier over the consumers) into the chunk's statistics,
+// pass 2's producer warp combines a row's chunk statistics when the row changes
+// and hands (M, 1/S) to the consumers in the stage header.
+
+constexpr int kSpConsumers = 256;
+constexpr int kSpThreads = kSpConsumers + 32;
+constexpr int kSpWarps = kSpConsumers / 32;
+constexpr int kSpMaxStages = 8;
+
+struct SplitTile {  // the work of chunk j of the window
+  int64_t r, c0;
+  int w;            // columns in this chunk
+};
+
+template <typename T>
+__device__ __forceinline__ SplitTile split_tile(const SmKernelArgs& a, int64_t row0, int64_t nchunks, int64_t j) {
+  SplitTile t;
+  t.r = row0 + j / nchunks;
+  t.c0 = (j % nchunks) * chunk_cols<T>();
+  t.w = static_cast<int>(min(chunk_cols<T>(), a.cols - t.c0));
+  return t;
+}
+
+// Range [lo, hi) of the window's chunks owned by this CTA.
+__device__ __forceinline__ void split_range(int64_t total, int64_t* lo, int64_t* hi) {
+  const int64_t q = total / gridDim.x, rem = total % gridDim.x, b = blockIdx.x;
+  *lo = b * q + min(b, rem);
+  *hi = *lo + q + (b < rem ? 1 : 0);
+}
+
+template <typename T, bool STATS>
+__global__ void __launch_bounds__(kSpThreads)
+k_softmax_split_tma(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t nchunks, float2* stats, int stages) {
+  constexpr int VW = dev::Vec16<T>::N;
+  constexpr int SLICE = int(chunk_cols<T>()) / kSpWarps;  // columns per consumer warp
+  constexpr int NV = SLICE / 32 / VW;                      // fragments per lane
+  constexpr uint32_t kStageBytes = 2 * uint32_t(kChunkBytes);
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t full[kSpMaxStages];
+  __shared__ __align__(8) uint64_t empty[kSpMaxStages];
+  __shared__ float2 hdr[kSpMaxStages];     // pass 2: (M, 1/S) of the stage's row
+  __shared__ float2 part[2][kSpWarps];     // pass 1: per-warp slice statistics
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  int64_t lo, hi;
+  split_range(nrows * nchunks, &lo, &hi);
+  const int64_t mine = hi - lo;
+
+  if (tid == 0) {
+    for (int st = 0; st < stages; ++st) {
+      dev::mbar_init(&full[st], 1);
+      dev::mbar_init(&empty[st], kSpWarps);
+    }
+    dev::mbar_init_fence();
+  }
+  __syncthreads();
+  if (mine <= 0) return;
+
+  if (warp == kSpWarps) {
+    // ---- producer warp: lane 0 copies; pass 2 also combines row statistics ----
+    const T* data = static_cast<const T*>(a.data);
+    const T* bias = static_cast<const T*>(a.bias);
+    const uint64_t pol_data = STATS ? dev::policy_evict_last() : dev::policy_evict_first();
+    const uint64_t pol_keep = dev::policy_evict_last();
+    int64_t cur_row = -1;
+    float2 cur = make_float2(0.f, 0.f);
+    for (int64_t j = 0; j < mine; ++j) {
+      const SplitTile t = split_tile<T>(a, row0, nchunks, lo + j);
+      if (!STATS && t.r != cur_row) {
+        const float2* sp = stats + t.r * nchunks;
+        float M = -INFINITY;
+        for (int64_t q = lane; q < nchunks; q += 32) M = fmaxf(M, sp[q].x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float S = 0.f;
+        for (int64_t q = lane; q < nchunks; q += 32) {
+          const float2 p = sp[q];
+          if (p.x != -INFINITY) S += p.y * dev::ex2_approx((p.x - M) * dev::kLog2e);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+        cur = make_float2(M, 1.0f / S);
+        cur_row = t.r;
+      }
+      int stop = 0;
+      if (lane == 0) {
+        const int st = static_cast<int>(j % stages);
+        if (j >= stages && !dev::mbar_wait(&empty[st], static_cast<uint32_t>((j / stages - 1) & 1))) {
+          // consumers stopped: wait (bounded) for the copies still in flight
+          for (int64_t k = j - stages; k < j; ++k)
+            dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
+          stop = 1;
+        } else {
+          if (!STATS) hdr[st] = cur;
+          unsigned char* dst = smem + size_t(st) * kStageBytes;
+          const uint32_t bytes = uint32_t(t.w) * uint32_t(sizeof(T));
+          dev::mbar_arrive_expect_tx(&full[st], 2u * bytes);
+          dev::bulk_g2s(dst, data + t.r * a.cols + t.c0, bytes, &full[st], pol_data);
+          dev::bulk_g2s(dst + kChunkBytes, bias + bias_row(a, t.r) * a.cols + t.c0, bytes, &full[st], pol_keep);
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) break;  // the whole warp stops together
+    }
+    return;
+  }
+
+  // ---- consumers ----
+  T* out = static_cast<T*>(a.output);
+  for (int64_t i = 0; i < mine; ++i) {
+    const int st = static_cast<int>(i % stages);
+    bool ok = dev::mbar_wait(&full[st], static_cast<uint32_t>((i / stages) & 1));
+    // pass 1 meets the other consumer warps at a named barrier below, so all of
+    // them decide together whether to stop
+    if constexpr (STATS) ok = dev::named_barrier_and(2, kSpConsumers, ok);
+    else ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return;
+    const SplitTile t = split_tile<T>(a, row0, nchunks, lo + i);
+    const T* sd = reinterpret_cast<const T*>(smem + size_t(st) * kStageBytes);
+    const T* sb = reinterpret_cast<const T*>(smem + size_t(st) * kStageBytes + kChunkBytes);
+    float z[NV][VW];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const int c = warp * SLICE + (v * 32 + lane) * VW;
+      if (c < t.w) {
+        float b[VW];
+        dev::lds_unpack(sd + c, z[v]);
+        dev::lds_unpack(sb + c, b);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) z[v][e] += b[e];
+      } else {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) z[v][e] = -INFINITY;
+      }
+    }
+    float2 h = make_float2(0.f, 0.f);
+    if (!STATS) h = hdr[st];
+    __syncwarp();
+    if (lane == 0) dev::mbar_arrive(&empty[st]);
+
+    if constexpr (STATS) {
+      float m = -INFINITY;
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int e = 0; e < VW; ++e) m = fmaxf(m, z[v][e]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float sum = 0.f;
+      if (m != -INFINITY) {
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+#pragma unroll
+          for (int e = 0; e < VW; ++e) sum += dev::ex2_approx((z[v][e] - m) * dev::kLog2e);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      // combine the 8 slices (double-buffered by chunk parity)
+      if (lane == 0) part[i & 1][warp] = make_float2(m, sum);
+      dev::named_barrier_sync(1, kSpConsumers);
+      if (warp == 0) {
+        const float2 p = part[i & 1][lane & (kSpWarps - 1)];
+        float M = p.x;
+#pragma unroll
+        for (int o = kSpWarps / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float S = (p.x != -INFINITY) ? p.y * dev::ex2_approx((p.x - M) * dev::kLog2e) : 0.f;
+#pragma unroll
+        for (int o = kSpWarps / 2; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+        if (lane == 0) stats[t.r * nchunks + t.c0 / chunk_cols<T>()] = make_float2(M, S);
+      }
+    } else {
+      T* orow = out + t.r * a.cols + t.c0;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int c = warp * SLICE + (v * 32 + lane) * VW;
+        if (c < t.w) {
+          float y[VW];
+#pragma unroll
+          for (int e = 0; e < VW; ++e) y[e] = dev::ex2_approx((z[v][e] - h.x) * dev::kLog2e) * h.y;
+          dev::stg_pack_stream(orow + c, y);
+        }
+      }
+    }
   }
 }
 
@@ -455,13 +646,36 @@ bool vec_ok(const void* data, const void* bias, const void* out, int64_t cols) {
 template <typename T, int VW>
 cudaError_t launch_split(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_count, int l2_bytes,
                          cudaStream_t stream, int* launches) {
-  const int64_t nchunks = (a.cols + kChunk - 1) / kChunk;
+  const int64_t nchunks = (a.cols + chunk_cols<T>() - 1) / chunk_cols<T>();
   float2* stats = static_cast<float2*>(a.workspace);
   // rows per window: keep a window's data within 3/4 of L2 so that the second
   // read (normalize) hits L2
   const int64_t row_bytes = a.cols * int64_t(sizeof(T));
   const int64_t budget = std::max<int64_t>(int64_t(l2_bytes) * 3 / 4, 1);
   const int64_t win = std::max<int64_t>(1, budget / row_bytes);
+  if constexpr (VW > 1) {
+    if (EP_SM_TMA) {
+      const int stages = std::min<int>(kSpMaxStages, std::max<int>(2, int(EP_SM_SPLIT_STAGE_BUDGET / (2 * kChunkBytes))));
+      const size_t smem = size_t(stages) * 2 * kChunkBytes;
+      int per1 = 1, per2 = 1;
+      cudaError_t e = resident_ctas(reinterpret_cast<const void*>(k_softmax_split_tma<T, true>), kSpThreads, smem, &per1);
+      if (e == cudaSuccess)
+        e = resident_ctas(reinterpret_cast<const void*>(k_softmax_split_tma<T, false>), kSpThreads, smem, &per2);
+      if (e != cudaSuccess) return e;
+      for (int64_t r0 = 0; r0 < a.rows; r0 += win) {
+        const int64_t nr = std::min(win, a.rows - r0);
+        const int64_t total = nr * nchunks;
+        const unsigned g1 = static_cast<unsigned>(std::min<int64_t>(total, int64_t(sm_count) * per1));
+        const unsigned g2 = static_cast<unsigned>(std::min<int64_t>(total, int64_t(sm_count) * per2));
+        k_softmax_split_tma<T, true><<<g1, kSpThreads, smem, stream>>>(k, r0, nr, nchunks, stats, stages);
+        k_softmax_split_tma<T, false><<<g2, kSpThreads, smem, stream>>>(k, r0, nr, nchunks, stats, stages);
+        *launches += 2;
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+      }
+      return cudaSuccess;
+    }
+  }
   const int64_t cap = int64_t(sm_count) * 8 * 16;
   for (int64_t r0 = 0; r0 < a.rows; r0 += win) {
     const int64_t nr = std::min(win, a.rows - r0);
@@ -556,9 +770,10 @@ cudaError_t launch_t(const SoftmaxArgs& a, int sm_count, int l2_bytes, cudaStrea
 
 }  // namespace
 
-size_t softmax_workspace_bytes(DType, int64_t rows, int64_t cols) {
+size_t softmax_workspace_bytes(DType t, int64_t rows, int64_t cols) {
   if (rows <= 0 || cols <= kRowMax) return 0;
-  const int64_t nchunks = (cols + kChunk - 1) / kChunk;
+  const int64_t chunk = kChunkBytes / dtype_size(t);
+  const int64_t nchunks = (cols + chunk - 1) / chunk;
   return static_cast<size_t>(rows * nchunks) * sizeof(float2);
 }
 

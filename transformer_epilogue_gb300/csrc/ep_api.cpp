@@ -294,8 +294,8 @@ ep_status ep_bias_softmax_noalloc(ep_dtype t, const void* data, const int64_t* s
   if (need > cap)
     return fail(EP_ERR_WORKSPACE,
                 "bias_softmax_noalloc: this shape needs %zu bytes of split-row scratch, more than the fixed %zu "
-                "(rows * ceil(blockSize / 8192) must be <= %zu); use ep_bias_softmax with a workspace",
-                need, cap, cap / 8);
+                "(rows * ceil(blockSize / %d) must be <= %zu); use ep_bias_softmax with a workspace",
+                need, cap, t == EP_F32 ? 4096 : 8192, cap / 8);
   DevInfo dv;
   if (ep_status s = device_info(&dv); s != EP_OK) return s;
   void* scratch = nullptr;

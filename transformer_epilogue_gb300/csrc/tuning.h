@@ -37,6 +37,12 @@
 #define EP_SM_TMA_MIN_TPR 16
 #endif
 
+// Split-row softmax (rows longer than the row kernels hold): shared memory for
+// the stages of one CTA (each stage is a 16 KB data chunk + its 16 KB of bias).
+#ifndef EP_SM_SPLIT_STAGE_BUDGET
+#define EP_SM_SPLIT_STAGE_BUDGET (64 * 1024)
+#endif
+
 // BiasAdd / QuickGelu: shared memory for one CTA's stages, 0/1 staged kernel.
 #ifndef EP_EW_TMA_STAGE_BUDGET
 #define EP_EW_TMA_STAGE_BUDGET (64 * 1024)
