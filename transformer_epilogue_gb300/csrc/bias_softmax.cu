@@ -467,12 +467,15 @@ k_softmax_split_tma(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t n
 
   if (tid == 0) {
     for (int st = 0; st < stages; ++st) {
-      dev::mbar_init(&full[st], 1);
+      // pass 2: the producer arrives twice per stage (copies armed; header written)
+      dev::mbar_init(&full[st], STATS ? 1 : 2);
       dev::mbar_init(&empty[st], kSpWarps);
     }
     dev::mbar_init_fence();
   }
   __syncthreads();
+  // pass 1 lets the (programmatically dependent) pass 2 be scheduled as its CTAs retire
+  if (STATS) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (mine <= 0) return;
 
   if (warp == kSpWarps) {
@@ -481,44 +484,80 @@ k_softmax_split_tma(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t n
     const T* bias = static_cast<const T*>(a.bias);
     const uint64_t pol_data = STATS ? dev::policy_evict_last() : dev::policy_evict_first();
     const uint64_t pol_keep = dev::policy_evict_last();
+    // lane 0: fill stage j % stages with chunk j (waiting for it to be empty
+    // first); false if the consumers stopped
+    auto fill = [&](int64_t j) -> bool {
+      const int st = static_cast<int>(j % stages);
+      if (j >= stages && !dev::mbar_wait(&empty[st], static_cast<uint32_t>((j / stages - 1) & 1))) {
+        for (int64_t k = j - stages; k < j; ++k)
+          dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
+        return false;
+      }
+      const SplitTile t = split_tile<T>(a, row0, nchunks, lo + j);
+      unsigned char* dst = smem + size_t(st) * kStageBytes;
+      const uint32_t bytes = uint32_t(t.w) * uint32_t(sizeof(T));
+      dev::mbar_arrive_expect_tx(&full[st], 2u * bytes);
+      dev::bulk_g2s(dst, data + t.r * a.cols + t.c0, bytes, &full[st], pol_data);
+      dev::bulk_g2s(dst + kChunkBytes, bias + bias_row(a, t.r) * a.cols + t.c0, bytes, &full[st], pol_keep);
+      return true;
+    };
+    const int64_t pre = min(int64_t(stages), mine);
+    if (lane == 0)
+      for (int64_t j = 0; j < pre; ++j) fill(j);
+    if (STATS) {
+      if (lane == 0)
+        for (int64_t j = pre; j < mine; ++j)
+          if (!fill(j)) break;
+      return;
+    }
+
+    // pass 2: the statistics come from pass 1, which may still be finishing
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     int64_t cur_row = -1;
     float2 cur = make_float2(0.f, 0.f);
     for (int64_t j = 0; j < mine; ++j) {
-      const SplitTile t = split_tile<T>(a, row0, nchunks, lo + j);
-      if (!STATS && t.r != cur_row) {
-        const float2* sp = stats + t.r * nchunks;
-        float M = -INFINITY;
-        for (int64_t q = lane; q < nchunks; q += 32) M = fmaxf(M, sp[q].x);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float S = 0.f;
-        for (int64_t q = lane; q < nchunks; q += 32) {
-          const float2 p = sp[q];
-          if (p.x != -INFINITY) S += p.y * dev::ex2_approx((p.x - M) * dev::kLog2e);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-        cur = make_float2(M, 1.0f / S);
-        cur_row = t.r;
-      }
       int stop = 0;
+      if (j >= pre && lane == 0) stop = fill(j) ? 0 : 1;
+      if (__shfl_sync(0xffffffffu, stop, 0)) break;  // the whole warp stops together
+      const int64_t r = row0 + (lo + j) / nchunks;
+      if (r != cur_row) {
+        // M = max m_b, S = sum s_b e^(m_b - M) over the row's chunks, 8 pairs per
+        // lane in flight, merged online across blocks of 256 pairs
+        const float2* sp = stats + r * nchunks;
+        float M = -INFINITY, S = 0.f;
+        for (int64_t q0 = 0; q0 < nchunks; q0 += 256) {
+          float2 p[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int64_t q = q0 + u * 32 + lane;
+            p[u] = q < nchunks ? sp[q] : make_float2(-INFINITY, 0.f);
+          }
+          float mb = p[0].x;
+#pragma unroll
+          for (int u = 1; u < 8; ++u) mb = fmaxf(mb, p[u].x);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+          float sb = 0.f;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (p[u].x != -INFINITY) sb += p[u].y * dev::ex2_approx((p[u].x - mb) * dev::kLog2e);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sb += __shfl_xor_sync(0xffffffffu, sb, o);
+          const float Mn = fmaxf(M, mb);
+          if (Mn != -INFINITY) {
+            S = (M != -INFINITY ? S * dev::ex2_approx((M - Mn) * dev::kLog2e) : 0.f) +
+                (mb != -INFINITY ? sb * dev::ex2_approx((mb - Mn) * dev::kLog2e) : 0.f);
+          }
+          M = Mn;
+        }
+        cur = make_float2(M, 1.0f / S);
+        cur_row = r;
+      }
       if (lane == 0) {
         const int st = static_cast<int>(j % stages);
-        if (j >= stages && !dev::mbar_wait(&empty[st], static_cast<uint32_t>((j / stages - 1) & 1))) {
-          // consumers stopped: wait (bounded) for the copies still in flight
-          for (int64_t k = j - stages; k < j; ++k)
-            dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
-          stop = 1;
-        } else {
-          if (!STATS) hdr[st] = cur;
-          unsigned char* dst = smem + size_t(st) * kStageBytes;
-          const uint32_t bytes = uint32_t(t.w) * uint32_t(sizeof(T));
-          dev::mbar_arrive_expect_tx(&full[st], 2u * bytes);
-          dev::bulk_g2s(dst, data + t.r * a.cols + t.c0, bytes, &full[st], pol_data);
-          dev::bulk_g2s(dst + kChunkBytes, bias + bias_row(a, t.r) * a.cols + t.c0, bytes, &full[st], pol_keep);
-        }
+        hdr[st] = cur;
+        dev::mbar_arrive(&full[st]);  // releases the header with the second arrival
       }
-      if (__shfl_sync(0xffffffffu, stop, 0)) break;  // the whole warp stops together
     }
     return;
   }
@@ -668,7 +707,20 @@ cudaError_t launch_split(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_cou
         const unsigned g1 = static_cast<unsigned>(std::min<int64_t>(total, int64_t(sm_count) * per1));
         const unsigned g2 = static_cast<unsigned>(std::min<int64_t>(total, int64_t(sm_count) * per2));
         k_softmax_split_tma<T, true><<<g1, kSpThreads, smem, stream>>>(k, r0, nr, nchunks, stats, stages);
-        k_softmax_split_tma<T, false><<<g2, kSpThreads, smem, stream>>>(k, r0, nr, nchunks, stats, stages);
+        // pass 2 may start while pass 1 drains; it waits for pass 1 (griddepcontrol.wait)
+        // before reading the chunk statistics, and reads only data before that
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(g2);
+        cfg.blockDim = dim3(kSpThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, k_softmax_split_tma<T, false>, k, r0, nr, nchunks, stats, stages);
+        if (e != cudaSuccess) return e;
         *launches += 2;
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
