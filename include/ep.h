@@ -109,6 +109,32 @@ ep_status ep_skip_layer_norm(ep_dtype t,
                              ep_stream_t stream);
 
 /*
+ * SkipLayerNormalization with the RMS form and the per-row statistics.
+ *   The manifests' SkipLayerNormalization shaders carry a `simplified` flag
+ *   (always false in the package; the RMS form of the contrib op family,
+ *   SkipSimplifiedLayerNormalization), and the op's `description` names the
+ *   training-statistics outputs it does not implement.  This entry point adds
+ *   both to ep_skip_layer_norm (same arguments, layout and errors otherwise):
+ *
+ * simplified   0: as ep_skip_layer_norm.  1: RMS form, no mean subtraction:
+ *              output = s / sqrt(mean(s^2) + epsilon) * gamma (+ beta)
+ *              (beta is normally NULL in this form).
+ * mean         NULL, or numel(input)/H float32 values: the mean of each row's s
+ *              (0 when simplified).
+ * inv_std_dev  NULL, or numel(input)/H float32 values: 1/sqrt(var + epsilon)
+ *              (1/sqrt(mean(s^2) + epsilon) when simplified).
+ * The float32 outputs must be 4-byte aligned and overlap no other operand.
+ */
+ep_status ep_skip_layer_norm_ex(ep_dtype t,
+                                const void* input, const int64_t* in_shape, int in_rank,
+                                const void* skip, const int64_t* skip_shape, int skip_rank,
+                                const void* gamma, const void* beta, const void* bias,
+                                float epsilon, int simplified,
+                                void* output, void* input_skip_bias_sum,
+                                float* mean, float* inv_std_dev,
+                                ep_stream_t stream);
+
+/*
  * BiasSoftmax
  *   com.microsoft.BiasSoftmax manifest: `description`, `attributes.axis`,
  *   `attributeDescriptions.is_inner_broadcast`, `derive` (axisNorm, batchCount,

@@ -35,6 +35,14 @@ def sln(lib, t=F32, inp=A, in_shape=(4, 8), skip=B, skip_shape=(4, 8), gamma=C, 
     return lib.ep_skip_layer_norm(t, inp, s_in, r_in, skip, s_sk, r_sk, gamma, beta, bias, eps, out, res, None)
 
 
+def sln_ex(lib, t=F32, inp=A, in_shape=(4, 8), skip=B, skip_shape=(4, 8), gamma=C, beta=D, bias=E, eps=1e-12,
+           simplified=0, out=F, res=None, mean=None, inv=None):
+    s_in, r_in = shp(*in_shape)
+    s_sk, r_sk = shp(*skip_shape)
+    return lib.ep_skip_layer_norm_ex(t, inp, s_in, r_in, skip, s_sk, r_sk, gamma, beta, bias, eps, simplified,
+                                     out, res, mean, inv, None)
+
+
 def softmax(lib, t=F32, data=A, shape=(4, 8), bias=B, bias_numel=8, axis=1, inner=1, out=C, ws=None, wsb=0):
     s, r = shp(*shape)
     return lib.ep_bias_softmax(t, data, s, r, bias, bias_numel, axis, inner, out, ws, wsb, None)
@@ -95,6 +103,15 @@ def cases(lib):
         ("sln sum overlaps output", sln(lib, res=F + 8), INVALID),
         ("sln output aliases broadcast skip", sln(lib, in_shape=(2, 3, 8), skip_shape=(3, 8), out=B), INVALID),
         ("sln output right after input ok", sln(lib, out=A + n48), CUDA),
+        # --- SkipLayerNormalization, RMS form and statistics
+        ("sln_ex simplified ok", sln_ex(lib, simplified=1, beta=None), CUDA),
+        ("sln_ex simplified must be 0/1", sln_ex(lib, simplified=2), INVALID),
+        ("sln_ex statistics ok", sln_ex(lib, mean=G, inv=G + 4096), CUDA),
+        ("sln_ex misaligned mean", sln_ex(lib, mean=G + 2), INVALID),
+        ("sln_ex mean overlaps inv_std_dev", sln_ex(lib, mean=G, inv=G + 8), INVALID),
+        ("sln_ex mean overlaps output", sln_ex(lib, mean=F + 4), INVALID),
+        ("sln_ex inv_std_dev overlaps input", sln_ex(lib, inv=A), INVALID),
+        ("sln_ex bf16 unsupported", sln_ex(lib, t=BF16), UNSUPPORTED),
         # --- BiasSoftmax
         ("softmax bf16 unsupported", softmax(lib, t=BF16), UNSUPPORTED),
         ("softmax rank 0", softmax(lib, shape=()), INVALID),

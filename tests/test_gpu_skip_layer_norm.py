@@ -231,3 +231,55 @@ def test_staged_many_tiles(lib, dtype, H, rows, skip_rows):
     out, s = run(lib, d, residual=True)
     sample = sorted(set(synth.sample_rows(rows, 1500)) | set(range(rows - 9, rows)))
     check(d, out, s, rows=sample)
+
+
+# ---------------------------------------------------------------------------
+# ep_skip_layer_norm_ex: the RMS (simplified) form and the per-row statistics
+# ---------------------------------------------------------------------------
+
+def run_ex(lib, d, simplified, residual=True):
+    dev = {k: (d[k].cuda() if d[k] is not None else None) for k in ("input", "skip", "gamma", "beta", "bias")}
+    x = d["input"]
+    rows = x.numel() // x.shape[-1]
+    go = Guarded(x.shape, x.dtype)
+    gs = Guarded(x.shape, x.dtype) if residual else None
+    gm = Guarded((rows,), torch.float32)
+    gi = Guarded((rows,), torch.float32)
+    lib.ep_skip_layer_norm_ex(dev["input"], dev["skip"], dev["gamma"], dev["beta"], dev["bias"], d["epsilon"],
+                              simplified=simplified, output=go.tensor,
+                              input_skip_bias_sum=gs.tensor if gs else None,
+                              mean=gm.tensor, inv_std_dev=gi.tensor)
+    torch.cuda.synchronize()
+    for gd in (go, gs, gm, gi):
+        if gd is not None:
+            gd.check()
+    return go.tensor.cpu(), (gs.tensor.cpu() if gs else None), gm.tensor.cpu(), gi.tensor.cpu()
+
+
+@pytest.mark.parametrize("simplified", [False, True])
+@pytest.mark.parametrize("dtype,shape,skip_shape,beta,bias", [
+    ("f32", (19, 768), None, False, True),        # staged path
+    ("f16", (7, 4096), None, True, True),         # staged path, exact rows
+    ("f32", (5, 771), None, False, False),        # register path (H % 4 != 0)
+    ("f16", (3, 20000), None, False, True),       # three-pass path
+    ("f32", (4, 11, 1024), (11, 1024), True, False),  # broadcast skip
+])
+def test_ex_simplified_and_statistics(lib, simplified, dtype, shape, skip_shape, beta, bias):
+    d = synth.sln_inputs(shape, skip_shape, dtype, has_beta=beta, has_bias=bias, seed=shape[-1])
+    out, s, mean, inv = run_ex(lib, d, simplified)
+    o = oracle.skip_layer_norm(d["input"], d["skip"], d["gamma"], d["beta"], d["bias"], d["epsilon"],
+                               simplified=simplified)
+    H = shape[-1]
+    assert_norm_close(out.reshape(-1, H), o["output"], d["input"].dtype)
+    assert_bit_exact(s.reshape(-1, H), oracle.skip_bias_sum(d["input"], d["skip"], d["bias"]))
+    np.testing.assert_allclose(mean.numpy().astype(np.float64), o["mean"], rtol=2e-5, atol=2e-6)
+    np.testing.assert_allclose(inv.numpy().astype(np.float64), o["inv_std_dev"], rtol=2e-5, atol=0)
+    if simplified:
+        assert (mean == 0).all()
+
+
+def test_ex_default_matches_plain_entry_point(lib):
+    d = synth.sln_inputs((33, 1024), None, "f16", has_beta=True, has_bias=True, seed=4)
+    a, s_a = run(lib, d, residual=True)
+    b, s_b, _, _ = run_ex(lib, d, simplified=False)
+    assert torch.equal(a, b) and torch.equal(s_a, s_b)

@@ -41,6 +41,9 @@ _SIGNATURES = {
     "ep_abi_version": (ctypes.c_int, []),
     "ep_skip_layer_norm": (ctypes.c_int, [ctypes.c_int, _vp, _i64p, ctypes.c_int, _vp, _i64p, ctypes.c_int,
                                           _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp]),
+    "ep_skip_layer_norm_ex": (ctypes.c_int, [ctypes.c_int, _vp, _i64p, ctypes.c_int, _vp, _i64p, ctypes.c_int,
+                                             _vp, _vp, _vp, ctypes.c_float, ctypes.c_int, _vp, _vp, _vp, _vp,
+                                             _vp]),
     "ep_bias_softmax": (ctypes.c_int, [ctypes.c_int, _vp, _i64p, ctypes.c_int, _vp, ctypes.c_int64,
                                        ctypes.c_int, ctypes.c_int, _vp, _vp, ctypes.c_size_t, _vp]),
     "ep_bias_softmax_workspace_size": (ctypes.c_size_t, [ctypes.c_int, _i64p, ctypes.c_int, ctypes.c_int]),
@@ -147,6 +150,44 @@ def ep_skip_layer_norm(input, skip, gamma, beta=None, bias=None, epsilon=DEFAULT
                                 _ptr(output), _ptr(input_skip_bias_sum), _stream(stream, input.device))
     _check(st)
     return output, input_skip_bias_sum
+
+
+def ep_skip_layer_norm_ex(input, skip, gamma, beta=None, bias=None, epsilon=DEFAULT_EPSILON, simplified=False,
+                          output=None, input_skip_bias_sum=None, mean=None, inv_std_dev=None, stream=None):
+    """SkipLayerNormalization with the RMS form (``simplified``) and the
+    per-row float32 statistics.  ``mean`` / ``inv_std_dev``: tensors to fill,
+    True to allocate, or None.  Returns (output, input_skip_bias_sum, mean,
+    inv_std_dev), the last three None when not requested."""
+    lib = load_library()
+    for n, t in (("input", input), ("skip", skip), ("gamma", gamma)):
+        _cuda(n, t)
+    _cuda("beta", beta, True)
+    _cuda("bias", bias, True)
+    if output is None:
+        output = torch.empty_like(input)
+    _cuda("output", output)
+    if input_skip_bias_sum is True:
+        input_skip_bias_sum = torch.empty_like(input)
+    elif input_skip_bias_sum is False:
+        input_skip_bias_sum = None
+    _cuda("input_skip_bias_sum", input_skip_bias_sum, True)
+    rows = input.numel() // max(1, input.shape[-1])
+    stat_shape = tuple(input.shape[:-1]) + (1,)
+    if mean is True:
+        mean = torch.empty(stat_shape, dtype=torch.float32, device=input.device)
+    if inv_std_dev is True:
+        inv_std_dev = torch.empty(stat_shape, dtype=torch.float32, device=input.device)
+    for n, t in (("mean", mean), ("inv_std_dev", inv_std_dev)):
+        _cuda(n, t, True)
+        if t is not None and (t.dtype != torch.float32 or t.numel() != rows):
+            raise ValueError(f"{n} must be a float32 tensor of {rows} elements")
+    st = lib.ep_skip_layer_norm_ex(_dtype(input), _ptr(input), _shape(input.shape), input.dim(),
+                                   _ptr(skip), _shape(skip.shape), skip.dim(),
+                                   _ptr(gamma), _ptr(beta), _ptr(bias), float(epsilon), int(bool(simplified)),
+                                   _ptr(output), _ptr(input_skip_bias_sum), _ptr(mean), _ptr(inv_std_dev),
+                                   _stream(stream, input.device))
+    _check(st)
+    return output, input_skip_bias_sum, mean, inv_std_dev
 
 
 def ep_bias_softmax_workspace_size(dtype, shape, axis=DEFAULT_AXIS) -> int:

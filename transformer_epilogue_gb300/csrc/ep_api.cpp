@@ -128,10 +128,11 @@ uint64_t ep_kernel_launch_count(void) { return g_launches.load(std::memory_order
 
 int ep_abi_version(void) { return kAbiVersion; }
 
-ep_status ep_skip_layer_norm(ep_dtype t, const void* input, const int64_t* in_shape, int in_rank,
-                             const void* skip, const int64_t* skip_shape, int skip_rank,
-                             const void* gamma, const void* beta, const void* bias, float epsilon,
-                             void* output, void* input_skip_bias_sum, ep_stream_t stream) {
+ep_status ep_skip_layer_norm_ex(ep_dtype t, const void* input, const int64_t* in_shape, int in_rank,
+                                const void* skip, const int64_t* skip_shape, int skip_rank,
+                                const void* gamma, const void* beta, const void* bias, float epsilon,
+                                int simplified, void* output, void* input_skip_bias_sum, float* mean,
+                                float* inv_std_dev, ep_stream_t stream) {
   if (!valid_dtype(t)) return fail(EP_ERR_UNSUPPORTED, "skip_layer_norm: dtype %d is not float32/float16", int(t));
   if (in_rank != 2 && in_rank != 3)
     return fail(EP_ERR_UNSUPPORTED, "skip_layer_norm: input rank %d (rank 2 or 3 supported)", in_rank);
@@ -160,6 +161,8 @@ ep_status ep_skip_layer_norm(ep_dtype t, const void* input, const int64_t* in_sh
   dims_product(skip_shape, 0, skip_rank, &skip_numel);
   const int64_t skip_rows = skip_numel / H;
   if (!(epsilon >= 0.0f)) return fail(EP_ERR_INVALID_ARG, "skip_layer_norm: epsilon must be >= 0");
+  if (simplified != 0 && simplified != 1)
+    return fail(EP_ERR_INVALID_ARG, "skip_layer_norm: simplified must be 0 or 1");
   if (rows == 0) return ok();
   if (skip_rows == 0 || rows % skip_rows != 0)
     return fail(EP_ERR_INVALID_ARG, "skip_layer_norm: skip rows do not tile the input rows");
@@ -170,6 +173,8 @@ ep_status ep_skip_layer_norm(ep_dtype t, const void* input, const int64_t* in_sh
   for (const void* p : ptrs)
     if (p != nullptr && !aligned(p, es))
       return fail(EP_ERR_INVALID_ARG, "skip_layer_norm: pointer %p is not aligned to the element size", p);
+  if ((mean != nullptr && !aligned(mean, 4)) || (inv_std_dev != nullptr && !aligned(inv_std_dev, 4)))
+    return fail(EP_ERR_INVALID_ARG, "skip_layer_norm: mean / inv_std_dev must be 4-byte aligned");
   const int64_t nb = numel * es;
   const Span in{input, nb}, sk{skip, skip_numel * es}, g{gamma, H * es}, b{beta, H * es}, bi{bias, H * es};
   const Span outs[] = {{output, nb}, {input_skip_bias_sum, nb}};
@@ -180,13 +185,30 @@ ep_status ep_skip_layer_norm(ep_dtype t, const void* input, const int64_t* in_sh
       return fail(EP_ERR_INVALID_ARG, "skip_layer_norm: an output overlaps an input other than as an exact alias");
   }
   if (overlap(outs[0], outs[1])) return fail(EP_ERR_INVALID_ARG, "skip_layer_norm: output and input_skip_bias_sum overlap");
+  const Span stat_spans[] = {{mean, rows * 4}, {inv_std_dev, rows * 4}};
+  for (const Span& st : stat_spans) {
+    if (st.p == nullptr) continue;
+    if (overlap(st, in) || overlap(st, sk) || overlap(st, g) || overlap(st, b) || overlap(st, bi) ||
+        overlap(st, outs[0]) || overlap(st, outs[1]))
+      return fail(EP_ERR_INVALID_ARG, "skip_layer_norm: mean / inv_std_dev overlap another operand");
+  }
+  if (overlap(stat_spans[0], stat_spans[1]))
+    return fail(EP_ERR_INVALID_ARG, "skip_layer_norm: mean and inv_std_dev overlap");
   DevInfo dv;
   if (ep_status s = device_info(&dv); s != EP_OK) return s;
-  ep::SlnArgs a{to_dtype(t), input, skip, gamma, beta, bias, output, input_skip_bias_sum, nullptr, nullptr,
-                rows, skip_rows, H, epsilon, false};
+  ep::SlnArgs a{to_dtype(t), input, skip, gamma, beta, bias, output, input_skip_bias_sum, mean, inv_std_dev,
+                rows, skip_rows, H, epsilon, simplified != 0};
   int launches = 0;
   cudaError_t e = ep::launch_skip_layer_norm(a, dv.sm_count, reinterpret_cast<cudaStream_t>(stream), &launches);
   return finish(e, launches, "skip_layer_norm");
+}
+
+ep_status ep_skip_layer_norm(ep_dtype t, const void* input, const int64_t* in_shape, int in_rank,
+                             const void* skip, const int64_t* skip_shape, int skip_rank,
+                             const void* gamma, const void* beta, const void* bias, float epsilon,
+                             void* output, void* input_skip_bias_sum, ep_stream_t stream) {
+  return ep_skip_layer_norm_ex(t, input, in_shape, in_rank, skip, skip_shape, skip_rank, gamma, beta, bias,
+                               epsilon, 0, output, input_skip_bias_sum, nullptr, nullptr, stream);
 }
 
 namespace {
