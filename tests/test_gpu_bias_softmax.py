@@ -208,3 +208,29 @@ def test_split_path_several_windows(lib, dtype, rows, cols, bias_rows, inner):
     sample = sorted(set(synth.sample_rows(rows, 12)) | {rows - 1})
     check(d["data"], d["bias"], 1, inner, out, rows=sample)
     np.testing.assert_allclose(to_np64(out).sum(axis=1), 1.0, atol=5e-3 if dtype == "f16" else 1e-4)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("cols", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("inner", [0, 1])
+def test_packed_rows(lib, dtype, cols, inner):
+    # rows of <= 8 elements: one thread per row
+    rows = 70007 if inner else 70000
+    bias_rows = 7 if inner else 16
+    d = synth.bias_softmax_inputs((rows, cols), (bias_rows, cols), dtype, data_std=3.0, seed=cols)
+    out = run(lib, d["data"], d["bias"], 1, inner)
+    sample = sorted(set(synth.sample_rows(rows, 3000)) | set(range(rows - 5, rows)))
+    check(d["data"], d["bias"], 1, inner, out, rows=sample)
+
+
+def test_packed_rows_bias_map_bit_exact(lib):
+    rows, cols, bias_rows = 4096, 8, 8
+    for inner in (0, 1):
+        data = torch.zeros(rows, cols)
+        bias = torch.full((bias_rows, cols), synth.MASKED)
+        bias[torch.arange(bias_rows), torch.arange(bias_rows)] = 0.0
+        out = run(lib, data, bias, 1, inner)
+        br = oracle.bias_row_of(np.arange(rows), bias_rows, rows // bias_rows, inner)
+        want = torch.zeros(rows, cols)
+        want[torch.arange(rows), torch.from_numpy(br)] = 1.0
+        assert torch.equal(out, want)

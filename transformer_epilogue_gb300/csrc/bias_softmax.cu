@@ -129,6 +129,57 @@ k_bias_softmax_rows(const SmKernelArgs a) {
 }
 
 // ---------------------------------------------------------------------------
+// Packed rows (blockSize <= 8, the manifest's `packed_rows` variant): one
+// thread per row, grid-stride over rows; the row's few elements stay in
+// registers.  Neighbouring threads read neighbouring rows, so a warp's loads
+// cover contiguous memory.
+// ---------------------------------------------------------------------------
+
+constexpr int kPackedMax = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(256) k_bias_softmax_packed(const SmKernelArgs a) {
+  const T* data = static_cast<const T*>(a.data);
+  const T* __restrict__ bias = static_cast<const T*>(a.bias);
+  T* out = static_cast<T*>(a.output);
+  const int C = static_cast<int>(a.cols);
+  const bool small = a.rows < (int64_t(1) << 31);
+  for (int64_t r = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; r < a.rows; r += int64_t(gridDim.x) * blockDim.x) {
+    int64_t br;
+    if (small) {  // 32-bit division when the indices fit
+      const uint32_t r32 = static_cast<uint32_t>(r);
+      br = a.inner ? r32 / static_cast<uint32_t>(a.inner_repeat) : r32 % static_cast<uint32_t>(a.bias_rows);
+    } else {
+      br = bias_row(a, r);
+    }
+    const T* d = data + r * C;
+    const T* b = bias + br * C;
+    float z[kPackedMax];
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kPackedMax; ++j) {
+      if (j < C) {
+        z[j] = dev::ld1_stream(d + j) + dev::ld1_keep(b + j);
+        m = fmaxf(m, z[j]);
+      }
+    }
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < kPackedMax; ++j) {
+      if (j < C) {
+        z[j] = __expf(z[j] - m);
+        sum += z[j];
+      }
+    }
+    const float inv = 1.0f / sum;
+    T* o = out + r * C;
+#pragma unroll
+    for (int j = 0; j < kPackedMax; ++j)
+      if (j < C) dev::st1_stream(o + j, z[j] * inv);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Shared-memory-staged, warp-specialised row kernel (the fast path for
 // 16-byte-aligned rows).
 //
@@ -801,6 +852,13 @@ cudaError_t launch_t(const SoftmaxArgs& a, int sm_count, int l2_bytes, cudaStrea
   constexpr int VW = dev::Vec16<T>::N;
   SmKernelArgs k{a.data, a.bias, a.output, a.rows, a.cols, a.bias_rows, a.inner_repeat, a.inner};
   const bool vec = vec_ok<T>(a.data, a.bias, a.output, a.cols);
+  if (a.cols <= kPackedMax) {
+    const int64_t blocks = (a.rows + 255) / 256;
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>(blocks, int64_t(sm_count) * 32));
+    k_bias_softmax_packed<T><<<grid, 256, 0, stream>>>(k);
+    *launches += 1;
+    return cudaGetLastError();
+  }
   if (vec && EP_SM_TMA) {
     cudaError_t e = cudaSuccess;
     if (launch_tma_rows<T>(k, a, sm_count, stream, launches, &e)) return e;
