@@ -24,7 +24,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-DTYPES = {"f32": torch.float32, "f16": torch.float16}
+DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
 # Attribute defaults printed by the op definitions:
 #   com.microsoft.QuickGelu manifest, `attributes.alpha`            -> 1.702

@@ -34,8 +34,8 @@
  *  - An output may alias an input exactly (same address, same size: in place).
  *    Any other overlap between an output and another operand is rejected.
  *  - Counts and offsets are 64-bit.
- *  - Arithmetic is float32 for both element types; float16 results are
- *    rounded once, to nearest-even, when stored.
+ *  - Arithmetic is float32 for every element type; float16 and bfloat16
+ *    results are rounded once, to nearest-even, when stored.
  */
 #ifndef TRANSFORMER_EPILOGUE_EP_H
 #define TRANSFORMER_EPILOGUE_EP_H
@@ -50,9 +50,11 @@ extern "C" {
 /* A CUDA stream; the same type as cudaStream_t (struct CUstream_st*). */
 typedef struct CUstream_st* ep_stream_t;
 
-/* Element type T.  The op definitions' typeConstraints list float32 and
- * float16 (typeConstraints of all four manifests). */
-typedef enum { EP_F32 = 0, EP_F16 = 1 } ep_dtype;
+/* Element type T.  The manifests' typeConstraints list float32 and float16
+ * (typeConstraints of all four manifests); the op schemas also allow
+ * bfloat16, which the WebGPU package leaves out (QuickGelu and
+ * SkipLayerNormalization `description`) and this library implements. */
+typedef enum { EP_F32 = 0, EP_F16 = 1, EP_BF16 = 2 } ep_dtype;
 
 typedef enum {
   EP_OK = 0,
@@ -95,7 +97,7 @@ int ep_abi_version(void);
  * output     shape of input.
  * input_skip_bias_sum   shape of input, or NULL.
  *
- * Errors: EP_ERR_UNSUPPORTED for a dtype other than EP_F32/EP_F16 or a rank
+ * Errors: EP_ERR_UNSUPPORTED for a dtype other than EP_F32/EP_F16/EP_BF16 or a rank
  * other than 2/3; EP_ERR_INVALID_ARG for a non-positive H, a skip shape not
  * listed above, a negative or NaN epsilon, a NULL required pointer, a
  * misaligned pointer or an overlap other than exact in-place aliasing.
@@ -186,7 +188,7 @@ size_t ep_bias_softmax_workspace_size(ep_dtype t, const int64_t* shape, int rank
  * The split-row scratch comes from a fixed 1 MiB device array inside the
  * library (held by every device that loads the library until process exit),
  * so rows * ceil(blockSize / chunk) must not exceed 131072 when blockSize >
- * 16384, with chunk = 4096 for float32 and 8192 for float16; larger shapes
+ * 16384, with chunk = 4096 for float32 and 8192 for float16/bfloat16; larger shapes
  * return EP_ERR_WORKSPACE before anything is enqueued.
  * Rows of up to 16384 elements need no scratch and have no such limit.
  * This entry point allocates nothing.

@@ -39,12 +39,20 @@ DEFAULT_ALPHA = 1.702                     # QuickGelu `attributes.alpha`
 DEFAULT_AXIS = 1                          # BiasSoftmax `attributes.axis`
 
 
+def _is_bf16(a):
+    return hasattr(a, "dtype") and str(a.dtype) == "torch.bfloat16"
+
+
 def _np(a):
-    """Accept NumPy arrays or CPU torch tensors; return a NumPy array."""
+    """Accept NumPy arrays or CPU torch tensors; return a NumPy array.  A
+    bfloat16 tensor (which NumPy has no type for) becomes float32, exactly."""
     if a is None:
         return None
     if hasattr(a, "detach"):
-        a = a.detach().cpu().numpy()
+        a = a.detach().cpu()
+        if _is_bf16(a):
+            a = a.float()
+        a = a.numpy()
     return np.asarray(a)
 
 
@@ -130,8 +138,11 @@ def skip_bias_sum(input, skip, bias=None, rows=None):
     Reading: the sum is evaluated in float32 in that order,
     f32(f32(input + skip) + bias), each step rounded to nearest-even, and the
     result is rounded once to T.  NumPy float32 arithmetic is IEEE
-    round-to-nearest-even, so it states the rounding exactly.
+    round-to-nearest-even, so it states the rounding exactly.  For bfloat16
+    the final rounding is torch's float32 -> bfloat16 conversion (also
+    nearest-even) and the result is a bfloat16 torch tensor.
     """
+    bf16 = _is_bf16(input)
     x = _np(input)
     sk = _np(skip)
     T = x.dtype
@@ -148,6 +159,9 @@ def skip_bias_sum(input, skip, bias=None, rows=None):
         if bb is not None:
             s = s + bb
         out[pos] = s.astype(T)
+    if bf16:
+        import torch
+        return torch.from_numpy(out).to(torch.bfloat16)
     return out
 
 

@@ -7,6 +7,12 @@ Tolerances (written out here, applied element by element):
     float16 spacing at |o| (2**(floor(log2|o|) - 10), at least 2**-24).  For
     |o| < 4 this is the literal 2e-3; above it, correct rounding alone can err
     by half a float16 spacing, which exceeds 2e-3 once |o| >= 8.
+  * bfloat16: |gpu - o| <= ulp_bf16(o), the bfloat16 spacing at |o|
+    (2**(floor(log2|o|) - 7), at least 2**-133): correct rounding (half a
+    spacing) plus the float32 arithmetic's error; for LayerNorm / softmax
+    outputs at least the float32 bound 1e-5, because where gamma*n cancels beta
+    the float32 arithmetic's own error (a few float32 ulps of the terms) is
+    larger than a bfloat16 spacing at the near-zero result.
   * the input_skip_bias_sum output and broadcast row indexing: bit-exact.
 ``o`` is always the oracle's unrounded float64 value.
 """
@@ -26,9 +32,23 @@ def ulp16(o):
     return np.maximum(2.0 ** (e - 10), 2.0 ** -24)
 
 
+def ulp_bf16(o):
+    a = np.abs(o)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.maximum(2.0 ** (e - 7), 2.0 ** -133)
+
+
 def to_np64(t: torch.Tensor) -> np.ndarray:
-    return t.detach().float().cpu().numpy().astype(np.float64) if t.dtype == torch.float16 \
-        else t.detach().cpu().numpy().astype(np.float64)
+    if t.dtype in (torch.float16, torch.bfloat16):
+        return t.detach().float().cpu().numpy().astype(np.float64)
+    return t.detach().cpu().numpy().astype(np.float64)
+
+
+def _low_tol(o, dtype, norm):
+    if dtype == torch.bfloat16:
+        return np.maximum(ulp_bf16(o), F32_ABS) if norm else ulp_bf16(o)
+    return np.maximum(F16_ABS, ulp16(o))
 
 
 def _report(bad, gpu, o, what):
@@ -44,7 +64,7 @@ def assert_norm_close(gpu: torch.Tensor, o: np.ndarray, dtype):
     if dtype == torch.float32:
         tol = np.full(o.shape, F32_ABS)
     else:
-        tol = np.maximum(F16_ABS, ulp16(o))
+        tol = _low_tol(o, dtype, norm=True)
     bad = ~both_nan & ~(np.abs(g - o) <= tol)
     assert not bad.any(), _report(bad, g, o, "norm/softmax")
     return float(np.nanmax(np.abs(g - o))) if o.size else 0.0
@@ -59,7 +79,7 @@ def assert_elementwise_close(gpu: torch.Tensor, o: np.ndarray, dtype):
         with np.errstate(invalid="ignore"):
             tol = F32_REL * np.abs(o) + TINY
     else:
-        tol = np.maximum(F16_ABS, ulp16(o))
+        tol = _low_tol(o, dtype, norm=False)
     with np.errstate(invalid="ignore"):
         bad = ~both_nan & ~same_inf & ~(np.abs(g - o) <= tol)
     assert not bad.any(), _report(bad, g, o, "elementwise")
@@ -67,7 +87,13 @@ def assert_elementwise_close(gpu: torch.Tensor, o: np.ndarray, dtype):
     return float(np.max(np.abs(g[fin] - o[fin]))) if fin.any() else 0.0
 
 
-def assert_bit_exact(gpu: torch.Tensor, want: np.ndarray):
+def assert_bit_exact(gpu: torch.Tensor, want):
+    if gpu.dtype == torch.bfloat16:
+        g16 = gpu.detach().cpu().reshape(-1).view(torch.int16)
+        w16 = torch.as_tensor(want).reshape(-1).view(torch.int16)
+        bad = (g16 != w16).numpy()
+        assert not bad.any(), f"{int(bad.sum())} bfloat16 elements differ bitwise, first at {np.argwhere(bad)[:5].tolist()}"
+        return
     g = gpu.detach().cpu().numpy()
     w = np.asarray(want).reshape(g.shape)
     assert g.dtype == w.dtype

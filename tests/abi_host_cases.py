@@ -67,7 +67,7 @@ def cases(lib):
     n48 = 4 * 8 * es32  # bytes of a (4, 8) f32 tensor
     return [
         # --- SkipLayerNormalization: dtype / rank
-        ("sln bf16 unsupported", sln(lib, t=BF16), UNSUPPORTED),
+        ("sln bf16 ok", sln(lib, t=BF16), CUDA),
         ("sln f64 unsupported", sln(lib, t=F64), UNSUPPORTED),
         ("sln rank 1 unsupported", sln(lib, in_shape=(8,), skip_shape=(8,)), UNSUPPORTED),
         ("sln rank 4 unsupported", sln(lib, in_shape=(1, 2, 4, 8), skip_shape=(1, 2, 4, 8)), UNSUPPORTED),
@@ -111,9 +111,10 @@ def cases(lib):
         ("sln_ex mean overlaps inv_std_dev", sln_ex(lib, mean=G, inv=G + 8), INVALID),
         ("sln_ex mean overlaps output", sln_ex(lib, mean=F + 4), INVALID),
         ("sln_ex inv_std_dev overlaps input", sln_ex(lib, inv=A), INVALID),
-        ("sln_ex bf16 unsupported", sln_ex(lib, t=BF16), UNSUPPORTED),
+        ("sln_ex f64 unsupported", sln_ex(lib, t=F64), UNSUPPORTED),
         # --- BiasSoftmax
-        ("softmax bf16 unsupported", softmax(lib, t=BF16), UNSUPPORTED),
+        ("softmax bf16 ok", softmax(lib, t=BF16), CUDA),
+        ("softmax f64 unsupported", softmax(lib, t=F64), UNSUPPORTED),
         ("softmax rank 0", softmax(lib, shape=()), INVALID),
         ("softmax rank 17 unsupported", softmax(lib, shape=(1,) * 17, bias_numel=1, axis=16), UNSUPPORTED),
         ("softmax axis = rank", softmax(lib, axis=2), INVALID),
@@ -154,7 +155,8 @@ def cases(lib):
         ("softmax noalloc in place ok", softmax_noalloc(lib, out=A), CUDA),
         ("softmax noalloc empty ok", softmax_noalloc(lib, shape=(0, 8), bias_numel=0, data=None, bias=None, out=None), OK),
         # --- BiasAdd
-        ("bias_add bf16 unsupported", bias_add(lib, t=BF16), UNSUPPORTED),
+        ("bias_add bf16 ok", bias_add(lib, t=BF16), CUDA),
+        ("bias_add f64 unsupported", bias_add(lib, t=F64), UNSUPPORTED),
         ("bias_add negative dim", bias_add(lib, shape=(2, -3, 8)), INVALID),
         ("bias_add empty ok", bias_add(lib, shape=(0, 3, 8), x=None, bias=None, skip=None, y=None), OK),
         ("bias_add NULL skip", bias_add(lib, skip=None), INVALID),
@@ -164,7 +166,8 @@ def cases(lib):
         ("bias_add Y overlaps bias", bias_add(lib, y=B), INVALID),
         ("bias_add Y partially overlaps X", bias_add(lib, y=A + 2), INVALID),
         # --- QuickGelu
-        ("gelu bf16 unsupported", gelu(lib, t=BF16), UNSUPPORTED),
+        ("gelu bf16 ok", gelu(lib, t=BF16), CUDA),
+        ("gelu f64 unsupported", gelu(lib, t=F64), UNSUPPORTED),
         ("gelu negative numel", gelu(lib, n=-1), INVALID),
         ("gelu empty ok", gelu(lib, n=0, x=None, y=None), OK),
         ("gelu NULL X", gelu(lib, x=None), INVALID),
@@ -197,8 +200,11 @@ def main():
     s, r = shp(262144, 512)
     if lib.ep_bias_softmax_workspace_size(F16, s, r, 1) != 0:
         bad.append(("workspace size of a row-path shape", 1, 0, ""))
-    if lib.ep_bias_softmax_workspace_size(BF16, s, r, 1) != 0:
+    if lib.ep_bias_softmax_workspace_size(F64, s, r, 1) != 0:
         bad.append(("workspace size of an unsupported dtype", 1, 0, ""))
+    s2, r2 = shp(2, 70000)
+    if lib.ep_bias_softmax_workspace_size(BF16, s2, r2, 1) != 2 * 9 * 8:   # bf16: 8192-column chunks
+        bad.append(("workspace size bf16 (2, 70000)", lib.ep_bias_softmax_workspace_size(BF16, s2, r2, 1), 144, ""))
     if lib.ep_kernel_launch_count() != n0:
         bad.append(("launch count moved", lib.ep_kernel_launch_count(), n0, ""))
     if lib.ep_abi_version() != 1:

@@ -388,3 +388,25 @@ def test_quick_gelu_worked_values_at_default_alpha():
 def test_quick_gelu_ieee_specials():
     out = oracle.quick_gelu(np.array([np.inf, -np.inf, np.nan], np.float32))
     assert out[0] == np.inf and np.isnan(out[1]) and np.isnan(out[2])
+
+
+def test_skip_bias_sum_bf16_rounds_to_nearest_even():
+    # bfloat16 spacing at 1 is 2^-7.  1 + 2^-8 is a tie that goes to the even
+    # neighbour 1; 1 + 2^-7 + 2^-8 is a tie between 1 + 2^-7 (odd) and
+    # 1 + 2^-6 (even).  Truncation would give 1 + 2^-7 for the second.
+    x = torch.tensor([[1.0, 1.0 + 2.0 ** -7]], dtype=torch.bfloat16)
+    sk = torch.tensor([[2.0 ** -8, 2.0 ** -8]], dtype=torch.bfloat16)
+    out = oracle.skip_bias_sum(x, sk)
+    assert out.dtype == torch.bfloat16
+    assert out.float().tolist() == [[1.0, 1.0 + 2.0 ** -6]]
+
+
+def test_bf16_inputs_enter_exactly():
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(5, 64, generator=g).to(torch.bfloat16)
+    sk = torch.randn(5, 64, generator=g).to(torch.bfloat16)
+    gm = torch.rand(64, generator=g).to(torch.bfloat16)
+    a = oracle.skip_layer_norm(x, sk, gm)["output"]
+    b = oracle.skip_layer_norm(x.float(), sk.float(), gm.float())["output"]
+    assert np.array_equal(a, b)
+    assert np.array_equal(oracle.quick_gelu(x), oracle.quick_gelu(x.float()))

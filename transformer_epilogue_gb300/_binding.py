@@ -224,7 +224,7 @@ def ep_bias_softmax_noalloc(data, bias, axis=DEFAULT_AXIS, is_inner_broadcast=No
     """BiasSoftmax for callers that cannot allocate device memory: the
     split-row scratch comes from a fixed 1 MiB array inside the library
     (rows * ceil(blockSize / chunk) <= 131072 when blockSize > 16384, chunk =
-    4096 for float32, 8192 for float16).  Calls
+    4096 for float32, 8192 for float16/bfloat16).  Calls
     that may overlap on the GPU share that array and must be ordered by the
     caller.  Pass ``output`` to keep the call free of allocations (otherwise
     PyTorch allocates it here).  Returns output."""

@@ -889,8 +889,11 @@ size_t softmax_workspace_bytes(DType t, int64_t rows, int64_t cols) {
 
 cudaError_t launch_bias_softmax(const SoftmaxArgs& a, int sm_count, int l2_bytes, cudaStream_t stream,
                                 int* launches) {
-  return a.t == DType::F32 ? launch_t<float>(a, sm_count, l2_bytes, stream, launches)
-                           : launch_t<__half>(a, sm_count, l2_bytes, stream, launches);
+  switch (a.t) {
+    case DType::F32: return launch_t<float>(a, sm_count, l2_bytes, stream, launches);
+    case DType::F16: return launch_t<__half>(a, sm_count, l2_bytes, stream, launches);
+    default: return launch_t<__nv_bfloat16>(a, sm_count, l2_bytes, stream, launches);
+  }
 }
 
 

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -15,6 +16,7 @@ namespace dev {
 template <typename T> struct Vec16;
 template <> struct Vec16<float> { static constexpr int N = 4; };
 template <> struct Vec16<__half> { static constexpr int N = 8; };
+template <> struct Vec16<__nv_bfloat16> { static constexpr int N = 8; };
 
 // ---------------------------------------------------------------------------
 // global memory access
@@ -35,39 +37,64 @@ __device__ __forceinline__ void st16_stream(void* p, uint4 v) {
 
 __device__ __forceinline__ float ld1_stream(const float* p) { return __ldcs(p); }
 __device__ __forceinline__ float ld1_stream(const __half* p) { return __half2float(__ldcs(p)); }
+__device__ __forceinline__ float ld1_stream(const __nv_bfloat16* p) { return __bfloat162float(__ldcs(p)); }
 __device__ __forceinline__ float ld1_keep(const float* p) { return __ldg(p); }
 __device__ __forceinline__ float ld1_keep(const __half* p) { return __half2float(__ldg(p)); }
+__device__ __forceinline__ float ld1_keep(const __nv_bfloat16* p) { return __bfloat162float(__ldg(p)); }
 __device__ __forceinline__ void st1_stream(float* p, float v) { __stcs(p, v); }
 __device__ __forceinline__ void st1_stream(__half* p, float v) { __stcs(p, __float2half_rn(v)); }
+__device__ __forceinline__ void st1_stream(__nv_bfloat16* p, float v) { __stcs(p, __float2bfloat16_rn(v)); }
 
-// 16 bytes <-> float32 lanes (conversions are exact for f16 -> f32; f32 -> f16
-// rounds to nearest-even).
-__device__ __forceinline__ void unpack(uint4 u, float (&f)[4]) {
-  f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
-  f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
-}
-__device__ __forceinline__ void unpack(uint4 u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
-    float2 t = __half22float2(h);
-    f[2 * i] = t.x; f[2 * i + 1] = t.y;
+// 16 bytes <-> float32 lanes, per element type (conversions to float32 are
+// exact; conversions from float32 round to nearest-even).
+template <typename T> struct Conv;
+template <> struct Conv<float> {
+  static __device__ __forceinline__ void unpack(uint4 u, float (&f)[4]) {
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
   }
-}
-__device__ __forceinline__ uint4 pack(const float (&f)[4]) {
-  return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
-                    __float_as_uint(f[2]), __float_as_uint(f[3]));
-}
-__device__ __forceinline__ uint4 pack(const float (&f)[8]) {
-  uint32_t w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
-    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  static __device__ __forceinline__ uint4 pack(const float (&f)[4]) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
   }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
+};
+template <> struct Conv<__half> {
+  static __device__ __forceinline__ void unpack(uint4 u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      f[2 * i] = t.x; f[2 * i + 1] = t.y;
+    }
+  }
+  static __device__ __forceinline__ uint4 pack(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+template <> struct Conv<__nv_bfloat16> {
+  static __device__ __forceinline__ void unpack(uint4 u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      f[2 * i] = t.x; f[2 * i + 1] = t.y;
+    }
+  }
+  static __device__ __forceinline__ uint4 pack(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
 
 // 2^x and 1/x with the hardware approximations (flush-to-zero): relative
 // errors of a few float32 ulp, used where the result is rounded to float16 or
@@ -84,14 +111,15 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
-// 16-byte shared-memory load, unpacked to float32.
-template <int VW>
-__device__ __forceinline__ void lds_unpack(const void* p, float (&f)[VW]) {
-  unpack(*reinterpret_cast<const uint4*>(p), f);
+// 16-byte shared-memory load of T elements, unpacked to float32; and a
+// 16-byte evict-first global store of float32 lanes packed to T.
+template <typename T, int VW>
+__device__ __forceinline__ void lds_unpack(const T* p, float (&f)[VW]) {
+  Conv<T>::unpack(*reinterpret_cast<const uint4*>(p), f);
 }
-template <int VW>
-__device__ __forceinline__ void stg_pack_stream(void* p, const float (&f)[VW]) {
-  st16_stream(p, pack(f));
+template <typename T, int VW>
+__device__ __forceinline__ void stg_pack_stream(T* p, const float (&f)[VW]) {
+  st16_stream(p, Conv<T>::pack(f));
 }
 
 // A fragment of VW consecutive elements held as float32.  VW == Vec16<T>::N
@@ -101,20 +129,15 @@ template <typename T, int VW> struct Frag {
   float v[VW];
   __device__ __forceinline__ void load_stream(const T* p) {
     if constexpr (VW == 1) v[0] = ld1_stream(p);
-    else unpack(ld16_stream(p), v);
+    else Conv<T>::unpack(ld16_stream(p), v);
   }
   __device__ __forceinline__ void load_keep(const T* p) {
     if constexpr (VW == 1) v[0] = ld1_keep(p);
-    else unpack(ld16_keep(p), v);
+    else Conv<T>::unpack(ld16_keep(p), v);
   }
   __device__ __forceinline__ void store_stream(T* p) const {
     if constexpr (VW == 1) st1_stream(p, v[0]);
-    else st16_stream(p, pack(v));
-  }
-  // 16-byte shared-memory load (VW == Vec16<T>::N only).
-  __device__ __forceinline__ void load_shared(const T* p) {
-    static_assert(VW > 1, "shared-memory fragments are 16 bytes");
-    unpack(*reinterpret_cast<const uint4*>(p), v);
+    else st16_stream(p, Conv<T>::pack(v));
   }
 };
 

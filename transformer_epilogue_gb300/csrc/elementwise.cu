@@ -13,6 +13,7 @@
 // reach 16-byte alignment) and a scalar tail.  Misaligned operands with
 // different offsets take the same kernel with VW = 1.
 #include <algorithm>
+#include <type_traits>
 
 #include "device_common.cuh"
 #include "ep_internal.h"
@@ -42,8 +43,11 @@ __device__ __forceinline__ float two_sum3(float a, float b, float c) {
 
 template <typename T>
 __device__ __forceinline__ float bias_add_elem(float x, float b, float s) {
-  if constexpr (sizeof(T) == 4) return two_sum3(x, b, s);
-  else return __fadd_rn(__fadd_rn(x, b), s);  // float16 terms: far below an f16 ulp
+  // float16 terms span at most 40 bits, so the float32 sum is within a float16
+  // ulp without compensation; float32 and bfloat16 (float32's exponent range)
+  // take the compensated sum.
+  if constexpr (std::is_same_v<T, __half>) return __fadd_rn(__fadd_rn(x, b), s);
+  else return two_sum3(x, b, s);
 }
 
 // BiasAdd: every fragment lies inside one row because C % VW == 0.
@@ -108,10 +112,12 @@ __device__ __forceinline__ float quick_gelu_f16(float x, float alpha) {
   return __fdividef(x, 1.0f + u);
 }
 
+// float16 results use the fast form; float32 and bfloat16 (whose range reaches
+// results far below the fast form's flush-to-zero threshold) the accurate one.
 template <typename T>
 __device__ __forceinline__ float quick_gelu_elem(float x, float alpha) {
-  if constexpr (sizeof(T) == 4) return quick_gelu_f32(x, alpha);
-  else return quick_gelu_f16(x, alpha);
+  if constexpr (std::is_same_v<T, __half>) return quick_gelu_f16(x, alpha);
+  else return quick_gelu_f32(x, alpha);
 }
 
 // Elements [0, head) and [head + nfrag*VW, n) are scalar; [head, head + nfrag*VW)
@@ -236,7 +242,8 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
       const float xv = dev::ld1_stream(x + e);
       float yv;
       if constexpr (BIAS_ADD) yv = bias_add_elem<T>(xv, dev::ld1_keep(bias + e % C), dev::ld1_stream(skip + e));
-      else yv = sizeof(T) == 4 ? quick_gelu_f32(xv, alpha) : quick_gelu_fast(xv, nal2e);
+      else if constexpr (!std::is_same_v<T, __half>) yv = quick_gelu_f32(xv, alpha);
+      else yv = quick_gelu_fast(xv, nal2e);
       dev::st1_stream(y + e, yv);
     }
   }
@@ -261,8 +268,8 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
     for (int u = 0; u < kEwFragsPerThread; ++u) {
       const int f = u * kEwConsumers + tid;
       if (f < nf) {
-        dev::lds_unpack(src + f * 16, a[u]);
-        if constexpr (BIAS_ADD) dev::lds_unpack(src + kTileBytes + f * 16, sk[u]);
+        dev::lds_unpack(reinterpret_cast<const T*>(src) + f * VW, a[u]);
+        if constexpr (BIAS_ADD) dev::lds_unpack(reinterpret_cast<const T*>(src + kTileBytes) + f * VW, sk[u]);
       }
     }
     __syncwarp();
@@ -281,7 +288,7 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
           dev::lds_unpack(reinterpret_cast<const T*>(smem) + c, b);
 #pragma unroll
           for (int e = 0; e < VW; ++e) a[u][e] = bias_add_elem<T>(a[u][e], b[e], sk[u][e]);
-        } else if constexpr (sizeof(T) == 4) {
+        } else if constexpr (!std::is_same_v<T, __half>) {
 #pragma unroll
           for (int e = 0; e < VW; ++e) a[u][e] = quick_gelu_f32(a[u][e], alpha);
         } else {
@@ -384,13 +391,19 @@ cudaError_t quick_gelu_t(const QuickGeluArgs& a, int sm_count, cudaStream_t stre
 }  // namespace
 
 cudaError_t launch_bias_add(const BiasAddArgs& a, int sm_count, cudaStream_t stream, int* launches) {
-  return a.t == DType::F32 ? bias_add_t<float>(a, sm_count, stream, launches)
-                           : bias_add_t<__half>(a, sm_count, stream, launches);
+  switch (a.t) {
+    case DType::F32: return bias_add_t<float>(a, sm_count, stream, launches);
+    case DType::F16: return bias_add_t<__half>(a, sm_count, stream, launches);
+    default: return bias_add_t<__nv_bfloat16>(a, sm_count, stream, launches);
+  }
 }
 
 cudaError_t launch_quick_gelu(const QuickGeluArgs& a, int sm_count, cudaStream_t stream, int* launches) {
-  return a.t == DType::F32 ? quick_gelu_t<float>(a, sm_count, stream, launches)
-                           : quick_gelu_t<__half>(a, sm_count, stream, launches);
+  switch (a.t) {
+    case DType::F32: return quick_gelu_t<float>(a, sm_count, stream, launches);
+    case DType::F16: return quick_gelu_t<__half>(a, sm_count, stream, launches);
+    default: return quick_gelu_t<__nv_bfloat16>(a, sm_count, stream, launches);
+  }
 }
 
 }  // namespace ep

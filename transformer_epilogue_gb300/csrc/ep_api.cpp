@@ -36,9 +36,11 @@ ep_status ok() {
   return EP_OK;
 }
 
-bool valid_dtype(ep_dtype t) { return t == EP_F32 || t == EP_F16; }
+bool valid_dtype(ep_dtype t) { return t == EP_F32 || t == EP_F16 || t == EP_BF16; }
 int esize(ep_dtype t) { return t == EP_F32 ? 4 : 2; }
-ep::DType to_dtype(ep_dtype t) { return t == EP_F32 ? ep::DType::F32 : ep::DType::F16; }
+ep::DType to_dtype(ep_dtype t) {
+  return t == EP_F32 ? ep::DType::F32 : t == EP_F16 ? ep::DType::F16 : ep::DType::BF16;
+}
 
 // Product of dims [b, e); false if a dim is negative or the product overflows 2^62.
 bool dims_product(const int64_t* d, int b, int e, int64_t* out) {
@@ -133,7 +135,7 @@ ep_status ep_skip_layer_norm_ex(ep_dtype t, const void* input, const int64_t* in
                                 const void* gamma, const void* beta, const void* bias, float epsilon,
                                 int simplified, void* output, void* input_skip_bias_sum, float* mean,
                                 float* inv_std_dev, ep_stream_t stream) {
-  if (!valid_dtype(t)) return fail(EP_ERR_UNSUPPORTED, "skip_layer_norm: dtype %d is not float32/float16", int(t));
+  if (!valid_dtype(t)) return fail(EP_ERR_UNSUPPORTED, "skip_layer_norm: dtype %d is not float32/float16/bfloat16", int(t));
   if (in_rank != 2 && in_rank != 3)
     return fail(EP_ERR_UNSUPPORTED, "skip_layer_norm: input rank %d (rank 2 or 3 supported)", in_rank);
   if (in_shape == nullptr || skip_shape == nullptr)
@@ -218,7 +220,7 @@ struct SoftmaxDims {
 };
 
 ep_status softmax_dims(const char* op, ep_dtype t, const int64_t* shape, int rank, int axis, SoftmaxDims* d) {
-  if (!valid_dtype(t)) return fail(EP_ERR_UNSUPPORTED, "%s: dtype %d is not float32/float16", op, int(t));
+  if (!valid_dtype(t)) return fail(EP_ERR_UNSUPPORTED, "%s: dtype %d is not float32/float16/bfloat16", op, int(t));
   if (rank < 1) return fail(EP_ERR_INVALID_ARG, "%s: data rank must be >= 1", op);
   if (rank > kMaxRank) return fail(EP_ERR_UNSUPPORTED, "%s: rank %d > %d", op, rank, kMaxRank);
   if (shape == nullptr) return fail(EP_ERR_INVALID_ARG, "%s: NULL shape array", op);
@@ -336,7 +338,7 @@ ep_status ep_bias_softmax_noalloc(ep_dtype t, const void* data, const int64_t* s
 
 ep_status ep_bias_add(ep_dtype t, const void* X, const int64_t* shape, const void* bias, const void* skip, void* Y,
                       ep_stream_t stream) {
-  if (!valid_dtype(t)) return fail(EP_ERR_UNSUPPORTED, "bias_add: dtype %d is not float32/float16", int(t));
+  if (!valid_dtype(t)) return fail(EP_ERR_UNSUPPORTED, "bias_add: dtype %d is not float32/float16/bfloat16", int(t));
   if (shape == nullptr) return fail(EP_ERR_INVALID_ARG, "bias_add: NULL shape array");
   int64_t n = 0;
   if (!dims_product(shape, 0, 3, &n)) return fail(EP_ERR_INVALID_ARG, "bias_add: negative or overflowing dims");
@@ -359,7 +361,7 @@ ep_status ep_bias_add(ep_dtype t, const void* X, const int64_t* shape, const voi
 }
 
 ep_status ep_quick_gelu(ep_dtype t, const void* X, int64_t numel, float alpha, void* Y, ep_stream_t stream) {
-  if (!valid_dtype(t)) return fail(EP_ERR_UNSUPPORTED, "quick_gelu: dtype %d is not float32/float16", int(t));
+  if (!valid_dtype(t)) return fail(EP_ERR_UNSUPPORTED, "quick_gelu: dtype %d is not float32/float16/bfloat16", int(t));
   if (numel < 0) return fail(EP_ERR_INVALID_ARG, "quick_gelu: negative numel");
   if (numel == 0) return ok();
   if (X == nullptr || Y == nullptr) return fail(EP_ERR_INVALID_ARG, "quick_gelu: X and Y are required");

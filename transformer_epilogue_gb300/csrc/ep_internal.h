@@ -12,7 +12,7 @@
 
 namespace ep {
 
-enum class DType : int { F32 = 0, F16 = 1 };
+enum class DType : int { F32 = 0, F16 = 1, BF16 = 2 };
 
 inline int dtype_size(DType t) { return t == DType::F32 ? 4 : 2; }
 

@@ -537,8 +537,11 @@ cudaError_t launch_t(const SlnArgs& a, int sm_count, cudaStream_t stream, int* l
 }  // namespace
 
 cudaError_t launch_skip_layer_norm(const SlnArgs& a, int sm_count, cudaStream_t stream, int* launches) {
-  return a.t == DType::F32 ? launch_t<float>(a, sm_count, stream, launches)
-                           : launch_t<__half>(a, sm_count, stream, launches);
+  switch (a.t) {
+    case DType::F32: return launch_t<float>(a, sm_count, stream, launches);
+    case DType::F16: return launch_t<__half>(a, sm_count, stream, launches);
+    default: return launch_t<__nv_bfloat16>(a, sm_count, stream, launches);
+  }
 }
 
 }  // namespace ep
