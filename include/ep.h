@@ -77,6 +77,24 @@ uint64_t ep_kernel_launch_count(void);
 /* Version of this ABI (incremented on any incompatible change). */
 int ep_abi_version(void);
 
+/* Failure detection.  Every shared-memory barrier wait in the staged kernels
+ * is bounded (1 s); a wait that runs out is counted on the device, the kernel
+ * stops its remaining work without leaving copies in flight, and the affected
+ * outputs are not written.  ep_pipeline_timeouts() adds up those counts on the
+ * current device into *count (0 when nothing timed out) and, if clear != 0,
+ * resets them.  It synchronises with the device.  No op definition covers
+ * this; it exists because the library's kernels wait on barriers. */
+ep_status ep_pipeline_timeouts(uint64_t* count, int clear);
+
+/* Self-test of that mechanism: launches a one-CTA kernel on `stream` whose
+ * barrier wait is set up to run out (it expects 16 bytes that no copy
+ * delivers) with a limit of timeout_us microseconds (1..1000000), waits for the
+ * stream, and stores in *timeouts_seen how many timed-out waits the library
+ * counted meanwhile (1 expected).  The kernel returns normally after the
+ * limit; the device stays usable.  EP_ERR_INVALID_ARG for a limit out of
+ * range or a NULL timeouts_seen. */
+ep_status ep_selftest_bounded_wait(uint32_t timeout_us, uint64_t* timeouts_seen, ep_stream_t stream);
+
 /*
  * SkipLayerNormalization
  *   com.microsoft.SkipLayerNormalization manifest: `description`, `inputs`,

@@ -154,6 +154,13 @@ def cases(lib):
         ("softmax noalloc contract", softmax_noalloc(lib, bias_numel=12), INVALID),
         ("softmax noalloc in place ok", softmax_noalloc(lib, out=A), CUDA),
         ("softmax noalloc empty ok", softmax_noalloc(lib, shape=(0, 8), bias_numel=0, data=None, bias=None, out=None), OK),
+        # --- failure detection
+        ("selftest limit 0", lib.ep_selftest_bounded_wait(0, ctypes.byref(ctypes.c_uint64()), None), INVALID),
+        ("selftest limit above 1 s", lib.ep_selftest_bounded_wait(1000001, ctypes.byref(ctypes.c_uint64()), None), INVALID),
+        ("selftest NULL result", lib.ep_selftest_bounded_wait(1000, None, None), INVALID),
+        ("selftest valid (no device)", lib.ep_selftest_bounded_wait(1000, ctypes.byref(ctypes.c_uint64()), None), CUDA),
+        ("pipeline_timeouts NULL", lib.ep_pipeline_timeouts(None, 0), INVALID),
+        ("pipeline_timeouts valid (no device)", lib.ep_pipeline_timeouts(ctypes.byref(ctypes.c_uint64()), 0), CUDA),
         # --- BiasAdd
         ("bias_add bf16 ok", bias_add(lib, t=BF16), CUDA),
         ("bias_add f64 unsupported", bias_add(lib, t=F64), UNSUPPORTED),

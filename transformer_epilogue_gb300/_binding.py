@@ -39,6 +39,8 @@ _SIGNATURES = {
     "ep_status_name": (ctypes.c_char_p, [ctypes.c_int]),
     "ep_kernel_launch_count": (ctypes.c_uint64, []),
     "ep_abi_version": (ctypes.c_int, []),
+    "ep_pipeline_timeouts": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint64), ctypes.c_int]),
+    "ep_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint64), _vp]),
     "ep_skip_layer_norm": (ctypes.c_int, [ctypes.c_int, _vp, _i64p, ctypes.c_int, _vp, _i64p, ctypes.c_int,
                                           _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp]),
     "ep_skip_layer_norm_ex": (ctypes.c_int, [ctypes.c_int, _vp, _i64p, ctypes.c_int, _vp, _i64p, ctypes.c_int,
@@ -125,6 +127,23 @@ def _cuda(name, t, optional=False):
 
 def kernel_launch_count() -> int:
     return int(load_library().ep_kernel_launch_count())
+
+
+def ep_pipeline_timeouts(clear=False) -> int:
+    """Bounded-wait timeouts the staged kernels counted on the current device
+    (synchronises with the device)."""
+    n = ctypes.c_uint64(0)
+    _check(load_library().ep_pipeline_timeouts(ctypes.byref(n), int(bool(clear))))
+    return int(n.value)
+
+
+def ep_selftest_bounded_wait(timeout_us=5000, stream=None) -> int:
+    """Run the failure-detection self-test; returns the timed-out waits counted
+    meanwhile (1 when the mechanism works)."""
+    n = ctypes.c_uint64(0)
+    _check(load_library().ep_selftest_bounded_wait(int(timeout_us), ctypes.byref(n),
+                                                   _stream(stream, torch.cuda.current_device())))
+    return int(n.value)
 
 
 def ep_skip_layer_norm(input, skip, gamma, beta=None, bias=None, epsilon=DEFAULT_EPSILON, output=None,

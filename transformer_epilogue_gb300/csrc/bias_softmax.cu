@@ -935,4 +935,6 @@ cudaError_t static_softmax_scratch(void** addr) {
   return cudaSuccess;
 }
 
+cudaError_t softmax_pipe_timeouts(unsigned int* count, bool clear) { return read_pipe_timeouts(count, clear); }
+
 }  // namespace ep

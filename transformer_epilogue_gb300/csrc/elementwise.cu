@@ -406,4 +406,26 @@ cudaError_t launch_quick_gelu(const QuickGeluArgs& a, int sm_count, cudaStream_t
   }
 }
 
+// Failure-detection self-test: one thread arms a shared-memory barrier for 16
+// bytes that no copy will deliver and waits for it with the given limit, so the
+// bounded wait runs out, is counted, and the kernel returns normally.  Nothing
+// is in flight when it exits.
+__global__ void k_selftest_bounded_wait(uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    dev::mbar_init(&bar, 1);
+    dev::mbar_init_fence();
+    dev::mbar_arrive_expect_tx(&bar, 16);
+    (void)dev::mbar_wait_for(&bar, 0, timeout_ns);
+  }
+}
+
+cudaError_t launch_selftest_bounded_wait(uint64_t timeout_ns, cudaStream_t stream, int* launches) {
+  k_selftest_bounded_wait<<<1, 32, 0, stream>>>(timeout_ns);
+  *launches += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t elementwise_pipe_timeouts(unsigned int* count, bool clear) { return read_pipe_timeouts(count, clear); }
+
 }  // namespace ep

@@ -130,6 +130,44 @@ uint64_t ep_kernel_launch_count(void) { return g_launches.load(std::memory_order
 
 int ep_abi_version(void) { return kAbiVersion; }
 
+namespace {
+cudaError_t sum_pipe_timeouts(unsigned int* total, bool clear) {
+  unsigned int a = 0, b = 0, c = 0;
+  cudaError_t e = ep::sln_pipe_timeouts(&a, clear);
+  if (e == cudaSuccess) e = ep::softmax_pipe_timeouts(&b, clear);
+  if (e == cudaSuccess) e = ep::elementwise_pipe_timeouts(&c, clear);
+  *total = a + b + c;
+  return e;
+}
+}  // namespace
+
+ep_status ep_pipeline_timeouts(uint64_t* count, int clear) {
+  if (count == nullptr) return fail(EP_ERR_INVALID_ARG, "pipeline_timeouts: NULL count");
+  unsigned int total = 0;
+  cudaError_t e = sum_pipe_timeouts(&total, clear != 0);
+  if (e != cudaSuccess) return fail(EP_ERR_CUDA, "pipeline_timeouts: %s", cudaGetErrorString(e));
+  *count = total;
+  return ok();
+}
+
+ep_status ep_selftest_bounded_wait(uint32_t timeout_us, uint64_t* timeouts_seen, ep_stream_t stream) {
+  if (timeouts_seen == nullptr) return fail(EP_ERR_INVALID_ARG, "selftest_bounded_wait: NULL timeouts_seen");
+  if (timeout_us < 1 || timeout_us > 1000000)
+    return fail(EP_ERR_INVALID_ARG, "selftest_bounded_wait: limit %u us outside 1..1000000", timeout_us);
+  unsigned int before = 0, after = 0;
+  cudaError_t e = sum_pipe_timeouts(&before, false);
+  if (e != cudaSuccess) return fail(EP_ERR_CUDA, "selftest_bounded_wait: %s", cudaGetErrorString(e));
+  int launches = 0;
+  e = ep::launch_selftest_bounded_wait(uint64_t(timeout_us) * 1000u, reinterpret_cast<cudaStream_t>(stream),
+                                       &launches);
+  g_launches.fetch_add(uint64_t(launches), std::memory_order_relaxed);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = sum_pipe_timeouts(&after, false);
+  if (e != cudaSuccess) return fail(EP_ERR_CUDA, "selftest_bounded_wait: %s", cudaGetErrorString(e));
+  *timeouts_seen = uint64_t(after - before);
+  return ok();
+}
+
 ep_status ep_skip_layer_norm_ex(ep_dtype t, const void* input, const int64_t* in_shape, int in_rank,
                                 const void* skip, const int64_t* skip_shape, int skip_rank,
                                 const void* gamma, const void* beta, const void* bias, float epsilon,

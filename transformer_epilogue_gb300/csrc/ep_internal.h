@@ -86,4 +86,13 @@ size_t softmax_workspace_bytes(DType t, int64_t rows, int64_t cols);
 size_t static_softmax_scratch_bytes();
 cudaError_t static_softmax_scratch(void** addr);
 
+// Bounded-wait timeouts counted by each translation unit's staged kernels on
+// the current device (synchronous read; `clear` resets the counter).
+cudaError_t sln_pipe_timeouts(unsigned int* count, bool clear);
+cudaError_t softmax_pipe_timeouts(unsigned int* count, bool clear);
+cudaError_t elementwise_pipe_timeouts(unsigned int* count, bool clear);
+
+// One-CTA kernel whose bounded wait is made to run out after timeout_ns.
+cudaError_t launch_selftest_bounded_wait(uint64_t timeout_ns, cudaStream_t stream, int* launches);
+
 }  // namespace ep

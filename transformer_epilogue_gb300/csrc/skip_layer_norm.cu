@@ -544,4 +544,6 @@ cudaError_t launch_skip_layer_norm(const SlnArgs& a, int sm_count, cudaStream_t 
   }
 }
 
+cudaError_t sln_pipe_timeouts(unsigned int* count, bool clear) { return read_pipe_timeouts(count, clear); }
+
 }  // namespace ep

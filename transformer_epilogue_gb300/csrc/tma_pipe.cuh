@@ -10,9 +10,10 @@
 // copy engine keeps up to S tiles per CTA in flight without holding registers.
 //
 // Every wait is bounded (kWaitTimeoutNs of %globaltimer): a wait that runs out
-// counts itself in g_pipe_timeouts (one counter per translation unit), and the
-// kernel then waits, again bounded, for its other copies in flight before it
-// returns, so no copy can land in shared memory the CTA no longer owns.
+// counts itself in g_pipe_timeouts (one counter per translation unit, read by
+// ep_pipeline_timeouts), and the kernel then waits, again bounded, for its
+// other copies in flight before it returns, so no copy can land in shared
+// memory the CTA no longer owns.
 #pragma once
 
 #include <cstdint>
@@ -66,19 +67,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits until the barrier's phase with the given parity has completed, for at
-// most kWaitTimeoutNs.  Returns false (and counts a timeout) if it ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// most timeout_ns.  Returns false (and counts a timeout) if it ran out.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+    if (global_timer_ns() - t0 > timeout_ns) {
       atomicAdd(&g_pipe_timeouts, 1u);
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_for(bar, parity, kWaitTimeoutNs);
 }
 
 // Plain arrive (release semantics: this thread's earlier shared-memory reads
@@ -138,10 +143,11 @@ __device__ __forceinline__ uint4 lds16(const void* p) {
 
 }  // namespace dev
 
-// Host side: read and clear this translation unit's timeout counter.
-static inline cudaError_t read_and_clear_pipe_timeouts(unsigned int* count) {
+// Host side: read (and optionally clear) this translation unit's timeout
+// counter on the current device.  Synchronous.
+static inline cudaError_t read_pipe_timeouts(unsigned int* count, bool clear) {
   cudaError_t e = cudaMemcpyFromSymbol(count, dev::g_pipe_timeouts, sizeof(unsigned int));
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || !clear) return e;
   const unsigned int zero = 0;
   return cudaMemcpyToSymbol(dev::g_pipe_timeouts, &zero, sizeof(unsigned int));
 }
