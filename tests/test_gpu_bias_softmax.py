@@ -210,6 +210,28 @@ def test_split_path_several_windows(lib, dtype, rows, cols, bias_rows, inner):
     np.testing.assert_allclose(to_np64(out).sum(axis=1), 1.0, atol=5e-3 if dtype == "f16" else 1e-4)
 
 
+@pytest.mark.parametrize("dtype,cols", [("f32", 40000), ("f16", 70000), ("bf16", 70000)])
+def test_split_ranges_cross_rows_with_masked_chunks(lib, dtype, cols):
+    # more chunks than one wave of CTAs, so a CTA's range of chunks runs from the
+    # tail of one row into the head of the next; whole chunks masked to -inf at
+    # the start, the end and the middle of rows, and one fully masked row
+    rows = 200
+    d = synth.bias_softmax_inputs((rows, cols), (rows, cols), dtype, data_std=2.0, seed=cols)
+    data = d["data"].clone()
+    chunk = 4096 if dtype == "f32" else 8192
+    for r in range(0, rows, 3):
+        data[r, :chunk + 7] = -float("inf")
+    for r in range(1, rows, 5):
+        data[r, cols - chunk - 3:] = -float("inf")
+    for r in range(2, rows, 7):
+        data[r, chunk:2 * chunk] = -float("inf")
+    data[rows // 2, :] = -float("inf")
+    out = run(lib, data, d["bias"], 1, 0)
+    live = [r for r in range(rows) if r != rows // 2]
+    check(data, d["bias"], 1, 0, out, rows=live)
+    assert torch.isnan(out[rows // 2]).all()
+
+
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
 @pytest.mark.parametrize("cols", [1, 2, 3, 5, 8])
 @pytest.mark.parametrize("inner", [0, 1])

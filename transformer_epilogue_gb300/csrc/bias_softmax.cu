@@ -239,9 +239,10 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
     const uint64_t pol_stream = dev::policy_evict_first();
     const uint64_t pol_keep = dev::policy_evict_last();
     const bool outer_all = !a.inner && a.bias_rows <= RT;
-    for (int64_t j = 0; j < mine; ++j) {
-      const int st = static_cast<int>(j % stages);
-      if (j >= stages && !dev::mbar_wait(&empty[st], static_cast<uint32_t>((j / stages - 1) & 1))) {
+    dev::Ring ring(stages);
+    for (int64_t j = 0; j < mine; ++j, ring.next()) {
+      const int st = ring.st;
+      if (j >= stages && !dev::mbar_wait(&empty[st], ring.phase ^ 1u)) {
         for (int64_t k = j - stages; k < j; ++k)
           dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
         return;
@@ -288,9 +289,10 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
   const int bar_id = 1 + g;
   const int gwarp0 = (g * TPR) >> 5;
 
-  for (int64_t i = 0; i < mine; ++i) {
-    const int st = static_cast<int>(i % stages);
-    bool ok = dev::mbar_wait(&full[st], static_cast<uint32_t>((i / stages) & 1));
+  dev::Ring ring(stages);
+  for (int64_t i = 0; i < mine; ++i, ring.next()) {
+    const int st = ring.st;
+    bool ok = dev::mbar_wait(&full[st], ring.phase);
     if constexpr (TPR > 32) ok = dev::named_barrier_and(bar_id, TPR, ok);
     else ok = __all_sync(0xffffffffu, ok);
     if (!ok) return;
@@ -464,32 +466,52 @@ k_softmax_chunk_normalize(const SmKernelArgs a, int64_t row0, int64_t nrows, int
   }
 }
 
-// Staged path (16-byte-aligned rows): warp-specialised, persistent, each CTA
+// Staged path (16-byte-aligned rows): warp-specialised and persistent, each CTA
 // owning a contiguous range of the window's chunks (so it meets few rows).  A
-// stage holds one chunk of data and the matching chunk of its bias row.  Each
-// of the 8 consumer warps reduces a 1/8 slice of the chunk; pass 1 combines the
-// slices (one named barrier over the consumers) into the chunk's statistics,
-// pass 2's producer warp combines a row's chunk statistics when the row changes
-// and hands (M, 1/S) to the consumers in the stage header.
+// chunk is streamed through shared memory as kSpTiles tiles; a stage holds one
+// tile of data and the matching tile of its bias row, so many small stages keep
+// enough bytes in flight per SM.  Each of the 8 consumer warps takes a 1/8 slice
+// of every tile.  Pass 1 keeps running statistics per lane and combines the
+// lanes and warps only where the CTA's part of a row ends; pass 2's producer
+// warp combines a row's chunk statistics when the row changes and hands
+// (M, 1/S) to the consumers in the stage header.
 
 constexpr int kSpConsumers = 256;
 constexpr int kSpThreads = kSpConsumers + 32;
 constexpr int kSpWarps = kSpConsumers / 32;
-constexpr int kSpMaxStages = 8;
+constexpr int kSpMaxStages = 16;
+constexpr int64_t kSpTileBytes = EP_SM_SPLIT_TILE_BYTES;
+constexpr int64_t kSpTiles = kChunkBytes / kSpTileBytes;  // tiles per chunk
+static_assert(kChunkBytes % kSpTileBytes == 0, "a chunk is a whole number of tiles");
+static_assert(kSpTileBytes % (kSpConsumers * 16) == 0, "every consumer lane takes whole 16-byte fragments");
+template <typename T> constexpr int sp_tile_cols() { return int(kSpTileBytes / int64_t(sizeof(T))); }
 
-struct SplitTile {  // the work of chunk j of the window
-  int64_t r, c0;
-  int w;            // columns in this chunk
+// Walks the tiles of a CTA's range in order: tile s of chunk kc of row r.
+struct SplitCursor {
+  int64_t r, kc;
+  int s;
+  __device__ __forceinline__ void start(int64_t row0, int64_t nchunks, int64_t chunk) {
+    r = row0 + chunk / nchunks;
+    kc = chunk % nchunks;
+    s = 0;
+  }
+  __device__ __forceinline__ void next(int64_t nchunks) {
+    if (++s == kSpTiles) {
+      s = 0;
+      if (++kc == nchunks) {
+        kc = 0;
+        ++r;
+      }
+    }
+  }
+  template <typename T> __device__ __forceinline__ int64_t col() const {
+    return kc * chunk_cols<T>() + int64_t(s) * sp_tile_cols<T>();
+  }
+  // columns in this tile (<= 0 past the end of the row)
+  template <typename T> __device__ __forceinline__ int width(int64_t cols) const {
+    return static_cast<int>(min(int64_t(sp_tile_cols<T>()), cols - col<T>()));
+  }
 };
-
-template <typename T>
-__device__ __forceinline__ SplitTile split_tile(const SmKernelArgs& a, int64_t row0, int64_t nchunks, int64_t j) {
-  SplitTile t;
-  t.r = row0 + j / nchunks;
-  t.c0 = (j % nchunks) * chunk_cols<T>();
-  t.w = static_cast<int>(min(chunk_cols<T>(), a.cols - t.c0));
-  return t;
-}
 
 // Range [lo, hi) of the window's chunks owned by this CTA.
 __device__ __forceinline__ void split_range(int64_t total, int64_t* lo, int64_t* hi) {
@@ -498,23 +520,59 @@ __device__ __forceinline__ void split_range(int64_t total, int64_t* lo, int64_t*
   *hi = *lo + q + (b < rem ? 1 : 0);
 }
 
+// z = data + bias for one lane's fragments of a staged tile (columns c0 +
+// v * 32 * VW); fragments at or past column `tw` are -inf unless WHOLE says the
+// tile is full.
+template <typename T, int NV, int VW, bool WHOLE>
+__device__ __forceinline__ void split_load_z(const T* sd, const T* sb, int c0, int tw, float (&z)[NV][VW]) {
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int c = c0 + v * 32 * VW;
+    if (WHOLE || c < tw) {
+      float b[VW];
+      dev::lds_unpack(sd + c, z[v]);
+      dev::lds_unpack(sb + c, b);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) z[v][e] += b[e];
+    } else {
+#pragma unroll
+      for (int e = 0; e < VW; ++e) z[v][e] = -INFINITY;
+    }
+  }
+}
+
+// y = e^(z - M) / S for one lane's fragments, stored where they lie in the row.
+template <typename T, int NV, int VW, bool WHOLE>
+__device__ __forceinline__ void split_store_y(T* orow, int c0, int tw, const float (&z)[NV][VW], float2 h) {
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int c = c0 + v * 32 * VW;
+    if (WHOLE || c < tw) {
+      float y[VW];
+#pragma unroll
+      for (int e = 0; e < VW; ++e) y[e] = dev::ex2_approx((z[v][e] - h.x) * dev::kLog2e) * h.y;
+      dev::stg_pack_stream(orow + c, y);
+    }
+  }
+}
+
 template <typename T, bool STATS>
 __global__ void __launch_bounds__(kSpThreads)
 k_softmax_split_tma(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t nchunks, float2* stats, int stages) {
   constexpr int VW = dev::Vec16<T>::N;
-  constexpr int SLICE = int(chunk_cols<T>()) / kSpWarps;  // columns per consumer warp
-  constexpr int NV = SLICE / 32 / VW;                      // fragments per lane
-  constexpr uint32_t kStageBytes = 2 * uint32_t(kChunkBytes);
+  constexpr int SLICE = sp_tile_cols<T>() / kSpWarps;  // columns per consumer warp
+  constexpr int NV = SLICE / 32 / VW;                   // fragments per lane
+  constexpr uint32_t kStageBytes = 2 * uint32_t(kSpTileBytes);
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[kSpMaxStages];
   __shared__ __align__(8) uint64_t empty[kSpMaxStages];
   __shared__ float2 hdr[kSpMaxStages];     // pass 2: (M, 1/S) of the stage's row
-  __shared__ float2 part[2][kSpWarps];     // pass 1: per-warp slice statistics
+  __shared__ float2 part[2][kSpWarps];     // pass 1: per-warp statistics of a row segment
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   int64_t lo, hi;
   split_range(nrows * nchunks, &lo, &hi);
-  const int64_t mine = hi - lo;
+  const int64_t mine = (hi - lo) * kSpTiles;  // tiles in the range
 
   if (tid == 0) {
     for (int st = 0; st < stages; ++st) {
@@ -535,30 +593,39 @@ k_softmax_split_tma(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t n
     const T* bias = static_cast<const T*>(a.bias);
     const uint64_t pol_data = STATS ? dev::policy_evict_last() : dev::policy_evict_first();
     const uint64_t pol_keep = dev::policy_evict_last();
-    // lane 0: fill stage j % stages with chunk j (waiting for it to be empty
-    // first); false if the consumers stopped
-    auto fill = [&](int64_t j) -> bool {
-      const int st = static_cast<int>(j % stages);
-      if (j >= stages && !dev::mbar_wait(&empty[st], static_cast<uint32_t>((j / stages - 1) & 1))) {
-        for (int64_t k = j - stages; k < j; ++k)
+    // lane 0: fill the next stage with tile n of the range (waiting for it to
+    // be empty first); false if the consumers stopped.  A tile past the end of
+    // its row completes its stage with no bytes.
+    SplitCursor fc;  // the tile the next fill copies
+    fc.start(row0, nchunks, lo);
+    dev::Ring fring(stages);  // its stage
+    auto fill = [&](int64_t n) -> bool {
+      const int st = fring.st;
+      if (n >= stages && !dev::mbar_wait(&empty[st], fring.phase ^ 1u)) {
+        for (int64_t k = n - stages; k < n; ++k)
           dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
         return false;
       }
-      const SplitTile t = split_tile<T>(a, row0, nchunks, lo + j);
+      const int w = fc.width<T>(a.cols);
       unsigned char* dst = smem + size_t(st) * kStageBytes;
-      const uint32_t bytes = uint32_t(t.w) * uint32_t(sizeof(T));
+      const uint32_t bytes = w > 0 ? uint32_t(w) * uint32_t(sizeof(T)) : 0u;
       dev::mbar_arrive_expect_tx(&full[st], 2u * bytes);
-      dev::bulk_g2s(dst, data + t.r * a.cols + t.c0, bytes, &full[st], pol_data);
-      dev::bulk_g2s(dst + kChunkBytes, bias + bias_row(a, t.r) * a.cols + t.c0, bytes, &full[st], pol_keep);
+      if (bytes) {
+        const int64_t c = fc.col<T>();
+        dev::bulk_g2s(dst, data + fc.r * a.cols + c, bytes, &full[st], pol_data);
+        dev::bulk_g2s(dst + kSpTileBytes, bias + bias_row(a, fc.r) * a.cols + c, bytes, &full[st], pol_keep);
+      }
+      fc.next(nchunks);
+      fring.next();
       return true;
     };
     const int64_t pre = min(int64_t(stages), mine);
     if (lane == 0)
-      for (int64_t j = 0; j < pre; ++j) fill(j);
+      for (int64_t n = 0; n < pre; ++n) fill(n);
     if (STATS) {
       if (lane == 0)
-        for (int64_t j = pre; j < mine; ++j)
-          if (!fill(j)) break;
+        for (int64_t n = pre; n < mine; ++n)
+          if (!fill(n)) break;
       return;
     }
 
@@ -566,11 +633,14 @@ k_softmax_split_tma(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t n
     asm volatile("griddepcontrol.wait;" ::: "memory");
     int64_t cur_row = -1;
     float2 cur = make_float2(0.f, 0.f);
-    for (int64_t j = 0; j < mine; ++j) {
+    SplitCursor hc;  // the tile whose header is written next
+    hc.start(row0, nchunks, lo);
+    dev::Ring hring(stages);
+    for (int64_t n = 0; n < mine; ++n, hc.next(nchunks), hring.next()) {
       int stop = 0;
-      if (j >= pre && lane == 0) stop = fill(j) ? 0 : 1;
+      if (n >= pre && lane == 0) stop = fill(n) ? 0 : 1;
       if (__shfl_sync(0xffffffffu, stop, 0)) break;  // the whole warp stops together
-      const int64_t r = row0 + (lo + j) / nchunks;
+      const int64_t r = hc.r;
       if (r != cur_row) {
         // M = max m_b, S = sum s_b e^(m_b - M) over the row's chunks, 8 pairs per
         // lane in flight, merged online across blocks of 256 pairs
@@ -579,19 +649,19 @@ k_softmax_split_tma(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t n
         for (int64_t q0 = 0; q0 < nchunks; q0 += 256) {
           float2 p[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int64_t q = q0 + u * 32 + lane;
-            p[u] = q < nchunks ? sp[q] : make_float2(-INFINITY, 0.f);
+          for (int k = 0; k < 8; ++k) {
+            const int64_t q = q0 + k * 32 + lane;
+            p[k] = q < nchunks ? sp[q] : make_float2(-INFINITY, 0.f);
           }
           float mb = p[0].x;
 #pragma unroll
-          for (int u = 1; u < 8; ++u) mb = fmaxf(mb, p[u].x);
+          for (int k = 1; k < 8; ++k) mb = fmaxf(mb, p[k].x);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
           float sb = 0.f;
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (p[u].x != -INFINITY) sb += p[u].y * dev::ex2_approx((p[u].x - mb) * dev::kLog2e);
+          for (int k = 0; k < 8; ++k)
+            if (p[k].x != -INFINITY) sb += p[k].y * dev::ex2_approx((p[k].x - mb) * dev::kLog2e);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) sb += __shfl_xor_sync(0xffffffffu, sb, o);
           const float Mn = fmaxf(M, mb);
@@ -605,7 +675,7 @@ k_softmax_split_tma(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t n
         cur_row = r;
       }
       if (lane == 0) {
-        const int st = static_cast<int>(j % stages);
+        const int st = hring.st;
         hdr[st] = cur;
         dev::mbar_arrive(&full[st]);  // releases the header with the second arrival
       }
@@ -614,80 +684,94 @@ k_softmax_split_tma(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t n
   }
 
   // ---- consumers ----
+  float ml = -INFINITY, sl = 0.f;  // pass 1: this lane's running (max, sum e^(z - max))
+  bool failed = false;             // this warp saw a wait run out: it reads no more stages
+  int seg = 0;
   T* out = static_cast<T*>(a.output);
-  for (int64_t i = 0; i < mine; ++i) {
-    const int st = static_cast<int>(i % stages);
-    bool ok = dev::mbar_wait(&full[st], static_cast<uint32_t>((i / stages) & 1));
-    // pass 1 meets the other consumer warps at a named barrier below, so all of
-    // them decide together whether to stop
-    if constexpr (STATS) ok = dev::named_barrier_and(2, kSpConsumers, ok);
-    else ok = __all_sync(0xffffffffu, ok);
-    if (!ok) return;
-    const SplitTile t = split_tile<T>(a, row0, nchunks, lo + i);
-    const T* sd = reinterpret_cast<const T*>(smem + size_t(st) * kStageBytes);
-    const T* sb = reinterpret_cast<const T*>(smem + size_t(st) * kStageBytes + kChunkBytes);
-    float z[NV][VW];
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      const int c = warp * SLICE + (v * 32 + lane) * VW;
-      if (c < t.w) {
-        float b[VW];
-        dev::lds_unpack(sd + c, z[v]);
-        dev::lds_unpack(sb + c, b);
-#pragma unroll
-        for (int e = 0; e < VW; ++e) z[v][e] += b[e];
-      } else {
-#pragma unroll
-        for (int e = 0; e < VW; ++e) z[v][e] = -INFINITY;
-      }
+  SplitCursor t;
+  t.start(row0, nchunks, lo);
+  dev::Ring ring(stages);
+  for (int64_t n = 0; n < mine; ++n, t.next(nchunks), ring.next()) {
+    const int st = ring.st;
+    const int tw = t.width<T>(a.cols);
+    if (!failed) failed = !__all_sync(0xffffffffu, dev::mbar_wait(&full[st], ring.phase));
+    if constexpr (!STATS) {
+      if (failed) return;  // pass 2's consumers never meet at a barrier
     }
-    float2 h = make_float2(0.f, 0.f);
-    if (!STATS) h = hdr[st];
-    __syncwarp();
-    if (lane == 0) dev::mbar_arrive(&empty[st]);
+    if (!failed) {
+      const T* sd = reinterpret_cast<const T*>(smem + size_t(st) * kStageBytes);
+      const T* sb = reinterpret_cast<const T*>(smem + size_t(st) * kStageBytes + kSpTileBytes);
+      const bool whole = tw == sp_tile_cols<T>();
+      const int c0 = warp * SLICE + lane * VW;
+      float z[NV][VW];
+      if (whole) split_load_z<T, NV, VW, true>(sd, sb, c0, tw, z);
+      else split_load_z<T, NV, VW, false>(sd, sb, c0, tw, z);
+      float2 h = make_float2(0.f, 0.f);
+      if (!STATS) h = hdr[st];
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(&empty[st]);
 
-    if constexpr (STATS) {
-      float m = -INFINITY;
-#pragma unroll
-      for (int v = 0; v < NV; ++v)
-#pragma unroll
-        for (int e = 0; e < VW; ++e) m = fmaxf(m, z[v][e]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      float sum = 0.f;
-      if (m != -INFINITY) {
+      if constexpr (STATS) {
+        float cm = -INFINITY;
 #pragma unroll
         for (int v = 0; v < NV; ++v)
 #pragma unroll
-          for (int e = 0; e < VW; ++e) sum += dev::ex2_approx((z[v][e] - m) * dev::kLog2e);
-      }
+          for (int e = 0; e < VW; ++e) cm = fmaxf(cm, z[v][e]);
+        const float mn = fmaxf(ml, cm);
+        if (mn != -INFINITY) {
+          float acc0 = sl * dev::ex2_approx((ml - mn) * dev::kLog2e);  // ml = -inf gives 0
+          float acc1 = 0.f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      // combine the 8 slices (double-buffered by chunk parity)
-      if (lane == 0) part[i & 1][warp] = make_float2(m, sum);
-      dev::named_barrier_sync(1, kSpConsumers);
-      if (warp == 0) {
-        const float2 p = part[i & 1][lane & (kSpWarps - 1)];
-        float M = p.x;
+          for (int v = 0; v < NV; ++v)
 #pragma unroll
-        for (int o = kSpWarps / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float S = (p.x != -INFINITY) ? p.y * dev::ex2_approx((p.x - M) * dev::kLog2e) : 0.f;
-#pragma unroll
-        for (int o = kSpWarps / 2; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-        if (lane == 0) stats[t.r * nchunks + t.c0 / chunk_cols<T>()] = make_float2(M, S);
-      }
-    } else {
-      T* orow = out + t.r * a.cols + t.c0;
-#pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        const int c = warp * SLICE + (v * 32 + lane) * VW;
-        if (c < t.w) {
-          float y[VW];
-#pragma unroll
-          for (int e = 0; e < VW; ++e) y[e] = dev::ex2_approx((z[v][e] - h.x) * dev::kLog2e) * h.y;
-          dev::stg_pack_stream(orow + c, y);
+            for (int e = 0; e < VW; e += 2) {
+              acc0 += dev::ex2_approx((z[v][e] - mn) * dev::kLog2e);
+              acc1 += dev::ex2_approx((z[v][e + 1] - mn) * dev::kLog2e);
+            }
+          sl = acc0 + acc1;
+          ml = mn;
         }
+      } else {
+        T* orow = out + t.r * a.cols + t.col<T>();
+        if (whole) split_store_y<T, NV, VW, true>(orow, c0, tw, z, h);
+        else split_store_y<T, NV, VW, false>(orow, c0, tw, z, h);
       }
+    }
+
+    if constexpr (STATS) {
+      // Where a chunk ends: if the CTA's part of the row ends too, combine the
+      // lanes and warps into the part's (max, sum) and store it as this chunk's
+      // statistics; otherwise store (-inf, 0), which pass 2's combine skips.
+      if (t.s != kSpTiles - 1) continue;
+      const bool seg_end = n + 1 == mine || t.kc + 1 == nchunks;
+      if (!seg_end) {
+        if (tid == 0) stats[t.r * nchunks + t.kc] = make_float2(-INFINITY, 0.f);
+        continue;
+      }
+      float M = ml;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float S = (ml != -INFINITY) ? sl * dev::ex2_approx((ml - M) * dev::kLog2e) : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+      // double-buffered by segment parity: warp 0 has read part[seg & 1] before
+      // it meets the next segment's barrier, which comes before any rewrite
+      if (lane == 0) part[seg & 1][warp] = make_float2(M, S);
+      // the consumers meet here only, and decide together whether to stop
+      if (!dev::named_barrier_and(2, kSpConsumers, !failed)) return;
+      if (warp == 0) {
+        const float2 p = part[seg & 1][lane & (kSpWarps - 1)];
+        float Mc = p.x;
+#pragma unroll
+        for (int o = kSpWarps / 2; o > 0; o >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, o));
+        float Sc = (p.x != -INFINITY) ? p.y * dev::ex2_approx((p.x - Mc) * dev::kLog2e) : 0.f;
+#pragma unroll
+        for (int o = kSpWarps / 2; o > 0; o >>= 1) Sc += __shfl_xor_sync(0xffffffffu, Sc, o);
+        if (lane == 0) stats[t.r * nchunks + t.kc] = make_float2(Mc, Sc);
+      }
+      ml = -INFINITY;
+      sl = 0.f;
+      ++seg;
     }
   }
 }
@@ -745,8 +829,8 @@ cudaError_t launch_split(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_cou
   const int64_t win = std::max<int64_t>(1, budget / row_bytes);
   if constexpr (VW > 1) {
     if (EP_SM_TMA) {
-      const int stages = std::min<int>(kSpMaxStages, std::max<int>(2, int(EP_SM_SPLIT_STAGE_BUDGET / (2 * kChunkBytes))));
-      const size_t smem = size_t(stages) * 2 * kChunkBytes;
+      const int stages = std::min<int>(kSpMaxStages, std::max<int>(2, int(EP_SM_SPLIT_STAGE_BUDGET / (2 * kSpTileBytes))));
+      const size_t smem = size_t(stages) * 2 * kSpTileBytes;
       int per1 = 1, per2 = 1;
       cudaError_t e = resident_ctas(reinterpret_cast<const void*>(k_softmax_split_tma<T, true>), kSpThreads, smem, &per1);
       if (e == cudaSuccess)

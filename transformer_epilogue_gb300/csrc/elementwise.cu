@@ -217,9 +217,10 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
       dev::mbar_arrive_expect_tx(&bias_bar, cb);
       dev::bulk_g2s(smem, bias, cb, &bias_bar, dev::policy_evict_last());
     }
-    for (int64_t j = 0; j < mine; ++j) {
-      const int st = static_cast<int>(j % stages);
-      if (j >= stages && !dev::mbar_wait(&empty[st], static_cast<uint32_t>((j / stages - 1) & 1))) {
+    dev::Ring ring(stages);
+    for (int64_t j = 0; j < mine; ++j, ring.next()) {
+      const int st = ring.st;
+      if (j >= stages && !dev::mbar_wait(&empty[st], ring.phase ^ 1u)) {
         if constexpr (BIAS_ADD) dev::mbar_wait(&bias_bar, 0);
         for (int64_t k = j - stages; k < j; ++k)
           dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
@@ -255,9 +256,10 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
     col_tile = static_cast<uint32_t>((int64_t(blockIdx.x) * kEwTileFrags * VW) % C);
   }
   const uint32_t Cu = static_cast<uint32_t>(C);
-  for (int64_t i = 0; i < mine; ++i) {
-    const int st = static_cast<int>(i % stages);
-    ok = dev::mbar_wait(&full[st], static_cast<uint32_t>((i / stages) & 1)) && ok;
+  dev::Ring ring(stages);
+  for (int64_t i = 0; i < mine; ++i, ring.next()) {
+    const int st = ring.st;
+    ok = dev::mbar_wait(&full[st], ring.phase) && ok;
     if (!__all_sync(0xffffffffu, ok)) return;
     const int64_t f0 = (blockIdx.x + i * gridDim.x) * int64_t(kEwTileFrags);
     const int nf = static_cast<int>(min(int64_t(kEwTileFrags), nfrag - f0));

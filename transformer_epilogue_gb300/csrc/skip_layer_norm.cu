@@ -282,9 +282,10 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
     dev::bulk_g2s(smem, a.gamma, row_bytes, &params_bar, pol_keep);
     if (has_beta) dev::bulk_g2s(smem + param_stride, a.beta, row_bytes, &params_bar, pol_keep);
     if (has_bias) dev::bulk_g2s(smem + param_stride * (1u + has_beta), a.bias, row_bytes, &params_bar, pol_keep);
-    for (int64_t j = 0; j < mine; ++j) {
-      const int st = static_cast<int>(j % stages);
-      if (j >= stages && !dev::mbar_wait(&empty[st], static_cast<uint32_t>((j / stages - 1) & 1))) {
+    dev::Ring ring(stages);
+    for (int64_t j = 0; j < mine; ++j, ring.next()) {
+      const int st = ring.st;
+      if (j >= stages && !dev::mbar_wait(&empty[st], ring.phase ^ 1u)) {
         // consumers stopped: wait (bounded) for the copies still in flight, then stop
         dev::mbar_wait(&params_bar, 0);
         for (int64_t k = j - stages; k < j; ++k)
@@ -321,9 +322,10 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
   const int gwarp0 = (g * TPR) >> 5;   // the group's first warp
   bool ok = dev::mbar_wait(&params_bar, 0);
 
-  for (int64_t i = 0; i < mine; ++i) {
-    const int st = static_cast<int>(i % stages);
-    ok = dev::mbar_wait(&full[st], static_cast<uint32_t>((i / stages) & 1)) && ok;
+  dev::Ring ring(stages);
+  for (int64_t i = 0; i < mine; ++i, ring.next()) {
+    const int st = ring.st;
+    ok = dev::mbar_wait(&full[st], ring.phase) && ok;
     if constexpr (TPR > 32) ok = dev::named_barrier_and(bar_id, TPR, ok);
     else ok = __all_sync(0xffffffffu, ok);
     if (!ok) return;

@@ -20,6 +20,8 @@
 
 #include <cuda_runtime.h>
 
+#include "tuning.h"
+
 namespace ep {
 namespace dev {
 
@@ -54,8 +56,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
       : "memory");
 }
 
+// One test of the phase; the thread may be suspended inside it until the
+// phase completes or, with EP_MBAR_SUSPEND_NS > 0, for at most that many ns.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t done;
+#if EP_MBAR_SUSPEND_NS > 0
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(uint32_t(EP_MBAR_SUSPEND_NS))
+      : "memory");
+#else
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -63,6 +76,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "=r"(done)
       : "r"(smem_addr(bar)), "r"(parity)
       : "memory");
+#endif
   return done != 0;
 }
 
@@ -135,6 +149,22 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
 }
+
+// Position in a ring of `n` stages: the stage of the current item and the
+// parity of that stage's current use (item i is in stage i % n, use i / n),
+// advanced one item at a time without a division.
+struct Ring {
+  int st = 0;
+  uint32_t phase = 0;
+  int n;
+  __device__ __forceinline__ explicit Ring(int stages) : n(stages) {}
+  __device__ __forceinline__ void next() {
+    if (++st == n) {
+      st = 0;
+      phase ^= 1u;
+    }
+  }
+};
 
 // 16-byte shared-memory load.
 __device__ __forceinline__ uint4 lds16(const void* p) {

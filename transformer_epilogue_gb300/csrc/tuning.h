@@ -3,6 +3,12 @@
 // values below are the library's defaults.
 #pragma once
 
+// Time limit (ns) handed to each mbarrier test of the staged kernels' waits;
+// 0 leaves it to the hardware.
+#ifndef EP_MBAR_SUSPEND_NS
+#define EP_MBAR_SUSPEND_NS 0
+#endif
+
 // SkipLayerNormalization: largest tile of rows per stage, shared memory for
 // one CTA's stages, minimum resident CTAs per SM the compiler must allow for
 // (register cap), and 0/1 to use the staged kernel at all.
@@ -37,8 +43,12 @@
 #define EP_SM_TMA_MIN_TPR 16
 #endif
 
-// Split-row softmax (rows longer than the row kernels hold): shared memory for
-// the stages of one CTA (each stage is a 16 KB data chunk + its 16 KB of bias).
+// Split-row softmax (rows longer than the row kernels hold): bytes of data in
+// one stage (4096, 8192 or 16384; the stage also holds as many bytes of bias),
+// and shared memory for the stages of one CTA.
+#ifndef EP_SM_SPLIT_TILE_BYTES
+#define EP_SM_SPLIT_TILE_BYTES 16384
+#endif
 #ifndef EP_SM_SPLIT_STAGE_BUDGET
 #define EP_SM_SPLIT_STAGE_BUDGET (64 * 1024)
 #endif
