@@ -23,6 +23,7 @@
 // The host runs the pair over windows of rows sized to stay resident in L2,
 // so the second read of a chunk is normally served from L2, not HBM.
 #include <algorithm>
+#include <climits>
 #include <atomic>
 #include <cmath>
 
@@ -190,10 +191,13 @@ __global__ void __launch_bounds__(256) k_bias_softmax_packed(const SmKernelArgs 
 //   inner broadcast: bias rows r0/ir .. (r0+nr-1)/ir, one contiguous copy;
 //   outer, biasRows <= RT: all bias rows;
 //   outer, biasRows > RT: bias rows (r0 + j) mod biasRows, one or two copies.
-// The producer also writes each row's bias slot into the stage's header, so
-// consumers do no index division.  `full`/`empty` mbarriers per stage hand
-// stages between producer and consumers; consumer groups synchronise only
-// among themselves.
+// The producer also writes the tile (-1: no more work) and each row's bias
+// slot into the stage's header, so consumers do no index division.
+// `full`/`empty` mbarriers per stage hand stages between producer and
+// consumers; consumer groups synchronise only among themselves.  With
+// EP_SM_CLC the grid has one CTA per tile and running CTAs take over the tiles
+// of CTAs they cancel (cluster launch control); otherwise a persistent grid
+// takes tiles round-robin.
 // ---------------------------------------------------------------------------
 
 constexpr int kWsConsumers = 256;
@@ -211,6 +215,9 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[kTmaMaxStages];
   __shared__ __align__(8) uint64_t empty[kTmaMaxStages];
+  __shared__ __align__(8) uint64_t clc_bar;
+  __shared__ __align__(16) uint4 clc_resp;
+  __shared__ int64_t tile_of[kTmaMaxStages];  // stage header: the tile, or -1
   __shared__ int slot_of[kTmaMaxStages][kMaxTileRows];
   __shared__ float red_a[kWsConsumerWarps];
   __shared__ float red_b[kWsConsumerWarps];
@@ -220,16 +227,17 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
   const uint32_t data_bytes = RT * row_bytes;
   const uint32_t stage_bytes = data_bytes + uint32_t(bias_slots) * row_bytes;
   const int tid = threadIdx.x;
-  const int64_t mine = ntiles > int64_t(blockIdx.x) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
   if (tid == 0) {
     for (int st = 0; st < stages; ++st) {
       dev::mbar_init(&full[st], 1);
       dev::mbar_init(&empty[st], kWsConsumerWarps);
     }
+    dev::mbar_init(&clc_bar, 1);
     dev::mbar_init_fence();
   }
   __syncthreads();
+  if (int64_t(blockIdx.x) >= ntiles) return;
 
   if (tid >= kWsConsumers) {
     // ---- producer ----
@@ -239,15 +247,26 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
     const uint64_t pol_stream = dev::policy_evict_first();
     const uint64_t pol_keep = dev::policy_evict_last();
     const bool outer_all = !a.inner && a.bias_rows <= RT;
+    // one CTA per tile: take over the tiles of cancelled CTAs; else round-robin
+    const bool use_clc = EP_SM_CLC && int64_t(gridDim.x) == ntiles;
+    dev::ClcStream clc(&clc_resp, &clc_bar);
+    if (use_clc) clc.request();
+    int64_t tile = blockIdx.x;
     dev::Ring ring(stages);
-    for (int64_t j = 0; j < mine; ++j, ring.next()) {
+    for (int64_t j = 0;; ++j, ring.next()) {
       const int st = ring.st;
       if (j >= stages && !dev::mbar_wait(&empty[st], ring.phase ^ 1u)) {
         for (int64_t k = j - stages; k < j; ++k)
           dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
+        clc.drain();
         return;
       }
-      const int64_t r0 = (blockIdx.x + j * gridDim.x) * RT;
+      tile_of[st] = tile;  // released to the consumers with the header below
+      if (tile < 0) {
+        dev::mbar_arrive(&full[st]);
+        break;
+      }
+      const int64_t r0 = tile * RT;
       const int nr = static_cast<int>(min(int64_t(RT), a.rows - r0));
       int64_t b0 = 0, n1 = 0, n2 = 0;  // bias rows [b0, b0+n1) then [0, n2)
       if (a.inner) {
@@ -278,7 +297,14 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
       dev::bulk_g2s(dst, data + r0 * C, uint32_t(nr) * row_bytes, &full[st], pol_stream);
       dev::bulk_g2s(bdst, bias + b0 * C, uint32_t(n1) * row_bytes, &full[st], pol_keep);
       if (n2 > 0) dev::bulk_g2s(bdst + n1 * row_bytes, bias, uint32_t(n2) * row_bytes, &full[st], pol_keep);
+      if (use_clc) {
+        tile = clc.next();
+      } else {
+        tile += gridDim.x;
+        if (tile >= ntiles) tile = -1;
+      }
     }
+    clc.drain();
     return;
   }
 
@@ -290,14 +316,16 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
   const int gwarp0 = (g * TPR) >> 5;
 
   dev::Ring ring(stages);
-  for (int64_t i = 0; i < mine; ++i, ring.next()) {
+  for (;; ring.next()) {
     const int st = ring.st;
     bool ok = dev::mbar_wait(&full[st], ring.phase);
     if constexpr (TPR > 32) ok = dev::named_barrier_and(bar_id, TPR, ok);
     else ok = __all_sync(0xffffffffu, ok);
     if (!ok) return;
+    const int64_t tile = tile_of[st];  // the same for every consumer
+    if (tile < 0) return;
 
-    const int64_t r = (blockIdx.x + i * gridDim.x) * RT + g;
+    const int64_t r = tile * RT + g;
     const bool active = r < a.rows;
     const unsigned char* stage = smem + size_t(st) * stage_bytes;
     const T* s_d = reinterpret_cast<const T*>(stage) + g * C;
@@ -924,7 +952,9 @@ bool launch_tma_rows(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_count, 
   *err = resident_ctas(reinterpret_cast<const void*>(f), kWsThreads, smem, &per_sm);
   if (*err != cudaSuccess) return true;
   const int64_t ntiles = (a.rows + rt - 1) / rt;
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(ntiles, int64_t(sm_count) * per_sm));
+  // one CTA per tile under launch control, else a persistent grid
+  const bool clc = EP_SM_CLC && ntiles <= int64_t(INT32_MAX);
+  const unsigned grid = static_cast<unsigned>(clc ? ntiles : std::min<int64_t>(ntiles, int64_t(sm_count) * per_sm));
   f<<<grid, kWsThreads, smem, stream>>>(k, stages, int(slots), ntiles);
   *launches += 1;
   *err = cudaGetLastError();

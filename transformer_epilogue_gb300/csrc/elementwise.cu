@@ -13,6 +13,7 @@
 // reach 16-byte alignment) and a scalar tail.  Misaligned operands with
 // different offsets take the same kernel with VW = 1.
 #include <algorithm>
+#include <climits>
 #include <type_traits>
 
 #include "device_common.cuh"
@@ -156,15 +157,19 @@ k_quick_gelu(const T* x, T* y, int64_t head, int64_t nfrag, int64_t n, float alp
 
 // ---------------------------------------------------------------------------
 // Shared-memory-staged, warp-specialised kernels (the fast path when every
-// operand is 16-byte aligned).  A persistent CTA has kEwConsumers consumer
-// threads and one producer warp; tiles are kEwTileFrags 16-byte fragments, and
-// each of its stages holds one tile of X (and of skip, for BiasAdd), filled by
-// the producer with cp.async.bulk copies.  `full`/`empty` mbarriers per stage
-// hand stages between producer and consumers, with no CTA-wide barrier.
-// BiasAdd's bias vector is bulk-copied into shared memory once per CTA; the
-// bias column of each fragment advances incrementally (no division per
-// fragment).  Elements after the last whole fragment are done by block 0's
-// consumers with scalar loads.
+// operand is 16-byte aligned).  A CTA has kEwConsumers consumer threads and one
+// producer warp; tiles are kEwTileFrags 16-byte fragments, and each of its
+// stages holds one tile of X (and of skip, for BiasAdd), filled by the producer
+// with cp.async.bulk copies, with a header naming the tile (-1: no more work)
+// and, for BiasAdd, the bias column of its first element.  `full`/`empty`
+// mbarriers per stage hand stages between producer and consumers, with no
+// CTA-wide barrier.  With EP_EW_CLC the grid has one CTA per tile and running
+// CTAs take over the tiles of CTAs they cancel (cluster launch control);
+// otherwise a persistent grid takes tiles round-robin.  BiasAdd's bias vector
+// is bulk-copied into shared memory once per CTA; within a tile the bias column
+// of each fragment advances incrementally (no division per fragment).
+// Elements after the last whole fragment are done by block 0's consumers with
+// scalar loads.
 // ---------------------------------------------------------------------------
 
 constexpr int kEwConsumers = 256;
@@ -184,7 +189,7 @@ __device__ __forceinline__ float quick_gelu_fast(float x, float nal2e) {
 template <typename T, bool BIAS_ADD>
 __global__ void __launch_bounds__(kEwThreads, EP_EW_TMA_MIN_CTAS)
 k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag, int64_t n, int64_t C,
-                  float alpha, int stages, uint32_t bias_bytes, uint32_t col_step_frag, uint32_t col_step_tile) {
+                  float alpha, int stages, uint32_t bias_bytes, uint32_t col_step_frag) {
   constexpr int VW = dev::Vec16<T>::N;
   constexpr int NOPS = BIAS_ADD ? 2 : 1;
   constexpr uint32_t kTileBytes = kEwTileFrags * 16u;
@@ -192,11 +197,14 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
   __shared__ __align__(8) uint64_t full[kEwMaxStages];
   __shared__ __align__(8) uint64_t empty[kEwMaxStages];
   __shared__ __align__(8) uint64_t bias_bar;
+  __shared__ __align__(8) uint64_t clc_bar;
+  __shared__ __align__(16) uint4 clc_resp;
+  __shared__ int64_t tile_of[kEwMaxStages];  // stage header: the tile, or -1
+  __shared__ uint32_t col_of[kEwMaxStages];  // BiasAdd: bias column of the tile's first element
   const int tid = threadIdx.x;
   unsigned char* stage0 = smem + bias_bytes;  // bias_bytes is a multiple of 128
   const uint32_t stage_bytes = NOPS * kTileBytes;
   const int64_t ntiles = (nfrag + kEwTileFrags - 1) / kEwTileFrags;
-  const int64_t mine = ntiles > int64_t(blockIdx.x) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
   if (tid == 0) {
     for (int st = 0; st < stages; ++st) {
@@ -204,35 +212,56 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
       dev::mbar_init(&empty[st], kEwConsumerWarps);
     }
     dev::mbar_init(&bias_bar, 1);
+    dev::mbar_init(&clc_bar, 1);
     dev::mbar_init_fence();
   }
   __syncthreads();
+  const bool have_tiles = int64_t(blockIdx.x) < ntiles;
 
   if (tid >= kEwConsumers) {
     // ---- producer ----
-    if (tid != kEwConsumers || mine == 0) return;
+    if (tid != kEwConsumers || !have_tiles) return;
     const uint64_t pol_stream = dev::policy_evict_first();
     if constexpr (BIAS_ADD) {
       const uint32_t cb = uint32_t(C) * uint32_t(sizeof(T));
       dev::mbar_arrive_expect_tx(&bias_bar, cb);
       dev::bulk_g2s(smem, bias, cb, &bias_bar, dev::policy_evict_last());
     }
+    // one CTA per tile: take over the tiles of cancelled CTAs; else round-robin
+    const bool use_clc = EP_EW_CLC && int64_t(gridDim.x) == ntiles;
+    dev::ClcStream clc(&clc_resp, &clc_bar);
+    if (use_clc) clc.request();
+    int64_t tile = blockIdx.x;
     dev::Ring ring(stages);
-    for (int64_t j = 0; j < mine; ++j, ring.next()) {
+    for (int64_t j = 0;; ++j, ring.next()) {
       const int st = ring.st;
       if (j >= stages && !dev::mbar_wait(&empty[st], ring.phase ^ 1u)) {
         if constexpr (BIAS_ADD) dev::mbar_wait(&bias_bar, 0);
         for (int64_t k = j - stages; k < j; ++k)
           dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
+        clc.drain();
         return;
       }
-      const int64_t f0 = (blockIdx.x + j * gridDim.x) * int64_t(kEwTileFrags);
+      tile_of[st] = tile;  // released to the consumers by the arrive below
+      if (tile < 0) {
+        dev::mbar_arrive(&full[st]);
+        break;
+      }
+      const int64_t f0 = tile * int64_t(kEwTileFrags);
+      if constexpr (BIAS_ADD) col_of[st] = static_cast<uint32_t>((f0 * VW) % C);
       const uint32_t bytes = static_cast<uint32_t>(min(int64_t(kEwTileFrags), nfrag - f0)) * 16u;
       unsigned char* dst = stage0 + size_t(st) * stage_bytes;
       dev::mbar_arrive_expect_tx(&full[st], NOPS * bytes);
       dev::bulk_g2s(dst, x + f0 * VW, bytes, &full[st], pol_stream);
       if constexpr (BIAS_ADD) dev::bulk_g2s(dst + kTileBytes, skip + f0 * VW, bytes, &full[st], pol_stream);
+      if (use_clc) {
+        tile = clc.next();
+      } else {
+        tile += gridDim.x;
+        if (tile >= ntiles) tile = -1;
+      }
     }
+    clc.drain();
     return;
   }
 
@@ -248,20 +277,19 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
       dev::st1_stream(y + e, yv);
     }
   }
-  if (mine == 0) return;
+  if (!have_tiles) return;
   bool ok = true;
-  uint32_t col_tile = 0;  // bias column of this CTA's current tile's first element
-  if constexpr (BIAS_ADD) {
-    ok = dev::mbar_wait(&bias_bar, 0);
-    col_tile = static_cast<uint32_t>((int64_t(blockIdx.x) * kEwTileFrags * VW) % C);
-  }
+  if constexpr (BIAS_ADD) ok = dev::mbar_wait(&bias_bar, 0);
   const uint32_t Cu = static_cast<uint32_t>(C);
   dev::Ring ring(stages);
-  for (int64_t i = 0; i < mine; ++i, ring.next()) {
+  for (;; ring.next()) {
     const int st = ring.st;
     ok = dev::mbar_wait(&full[st], ring.phase) && ok;
     if (!__all_sync(0xffffffffu, ok)) return;
-    const int64_t f0 = (blockIdx.x + i * gridDim.x) * int64_t(kEwTileFrags);
+    const int64_t tile = tile_of[st];  // the header is read before the stage is released
+    if (tile < 0) return;
+    const uint32_t col0 = BIAS_ADD ? col_of[st] : 0u;
+    const int64_t f0 = tile * int64_t(kEwTileFrags);
     const int nf = static_cast<int>(min(int64_t(kEwTileFrags), nfrag - f0));
     const unsigned char* src = stage0 + size_t(st) * stage_bytes;
     float a[kEwFragsPerThread][VW];
@@ -278,7 +306,7 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
     if ((tid & 31) == 0) dev::mbar_arrive(&empty[st]);
     uint32_t c = 0;
     if constexpr (BIAS_ADD) {
-      c = col_tile + uint32_t(tid) * VW;
+      c = col0 + uint32_t(tid) * VW;
       c = c % Cu;
     }
 #pragma unroll
@@ -304,10 +332,6 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
         if (c >= Cu) c -= Cu;
       }
     }
-    if constexpr (BIAS_ADD) {
-      col_tile += col_step_tile;
-      if (col_tile >= Cu) col_tile -= Cu;
-    }
   }
 }
 
@@ -328,12 +352,12 @@ cudaError_t launch_ew_tma(const T* x, const T* skip, const T* bias, T* y, int64_
   cudaError_t e = resident_ctas(reinterpret_cast<const void*>(fn), kEwThreads, smem, &per_sm);
   if (e != cudaSuccess) return e;
   const int64_t ntiles = (nfrag + kEwTileFrags - 1) / kEwTileFrags;
-  const unsigned grid =
-      static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(ntiles, int64_t(sm_count) * per_sm)));
+  // one CTA per tile under launch control, else a persistent grid
+  const bool clc = EP_EW_CLC && ntiles <= int64_t(INT32_MAX);
+  const unsigned grid = static_cast<unsigned>(
+      std::max<int64_t>(1, clc ? ntiles : std::min<int64_t>(ntiles, int64_t(sm_count) * per_sm)));
   const uint32_t step_frag = BIAS_ADD ? uint32_t((int64_t(kEwConsumers) * VW) % C) : 0u;
-  const uint32_t step_tile = BIAS_ADD ? uint32_t((int64_t(grid) * kEwTileFrags * VW) % C) : 0u;
-  fn<<<grid, kEwThreads, smem, stream>>>(x, skip, bias, y, nfrag, n, C, alpha, stages, bias_bytes, step_frag,
-                                         step_tile);
+  fn<<<grid, kEwThreads, smem, stream>>>(x, skip, bias, y, nfrag, n, C, alpha, stages, bias_bytes, step_frag);
   return cudaGetLastError();
 }
 

@@ -16,6 +16,7 @@
 // register budget fall back to a CTA-per-row kernel that re-reads the row
 // (three passes) instead of holding it.
 #include <algorithm>
+#include <climits>
 
 #include "device_common.cuh"
 #include "ep_internal.h"
@@ -217,16 +218,20 @@ __global__ void __launch_bounds__(1024) k_skip_layer_norm_long(const SlnKernelAr
 // Shared-memory-staged, warp-specialised kernel (the fast path for 16-byte-
 // aligned rows).
 //
-// A persistent CTA has kWsConsumers consumer threads in row groups of TPR and
-// one producer warp.  Tiles are RT = kWsConsumers/TPR consecutive rows; each of
-// the `stages` shared-memory stages holds one tile: the RT input rows, then the
-// RT skip rows (for a broadcast skip, rows r mod skipRows).  Per stage, `full`
-// completes when the producer's cp.async.bulk copies have landed and `empty`
-// when all consumer warps are done with it.  The producer refills a stage as
-// soon as it is empty, so up to `stages` tiles are in flight per CTA; consumer
-// groups synchronise only among themselves (shuffles, or a named barrier when a
-// row spans several warps), never CTA-wide.  The arithmetic is that of
-// k_skip_layer_norm, reading rows from shared memory.
+// A CTA has kWsConsumers consumer threads in row groups of TPR and one
+// producer warp.  Tiles are RT = kWsConsumers/TPR consecutive rows; each of the
+// `stages` shared-memory stages holds one tile: the RT input rows, then the RT
+// skip rows (for a broadcast skip, rows r mod skipRows), and the stage header
+// names the tile (-1: no more work).  Per stage, `full` completes when the
+// producer's cp.async.bulk copies have landed and `empty` when all consumer
+// warps are done with it.  The producer refills a stage as soon as it is empty,
+// so up to `stages` tiles are in flight per CTA; consumer groups synchronise
+// only among themselves (shuffles, or a named barrier when a row spans several
+// warps), never CTA-wide.  With EP_SLN_CLC the grid has one CTA per tile and
+// each running CTA takes over the tiles of CTAs it cancels (cluster launch
+// control), so faster SMs take more tiles; otherwise a persistent grid takes
+// tiles round-robin.  The arithmetic is that of k_skip_layer_norm, reading rows
+// from shared memory.
 // ---------------------------------------------------------------------------
 
 constexpr int kWsConsumers = 256;
@@ -246,6 +251,9 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
   __shared__ __align__(8) uint64_t full[kTmaMaxStages];
   __shared__ __align__(8) uint64_t empty[kTmaMaxStages];
   __shared__ __align__(8) uint64_t params_bar;
+  __shared__ __align__(8) uint64_t clc_bar;
+  __shared__ __align__(16) uint4 clc_resp;
+  __shared__ int64_t tile_of[kTmaMaxStages];  // stage header: the tile, or -1
   __shared__ float red_a[kWsConsumerWarps];
   __shared__ float red_b[kWsConsumerWarps];
 
@@ -258,7 +266,6 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
   const uint32_t param_bytes = param_stride * (1u + has_beta + has_bias);
   unsigned char* stage0 = smem + param_bytes;
   const int tid = threadIdx.x;
-  const int64_t mine = ntiles > int64_t(blockIdx.x) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
   if (tid == 0) {
     for (int st = 0; st < stages; ++st) {
@@ -266,10 +273,11 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
       dev::mbar_init(&empty[st], kWsConsumerWarps);
     }
     dev::mbar_init(&params_bar, 1);
+    dev::mbar_init(&clc_bar, 1);
     dev::mbar_init_fence();
   }
   __syncthreads();
-  if (mine == 0) return;
+  if (int64_t(blockIdx.x) >= ntiles) return;
 
   if (tid >= kWsConsumers) {
     // ---- producer: one thread issues every copy of this CTA ----
@@ -282,17 +290,28 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
     dev::bulk_g2s(smem, a.gamma, row_bytes, &params_bar, pol_keep);
     if (has_beta) dev::bulk_g2s(smem + param_stride, a.beta, row_bytes, &params_bar, pol_keep);
     if (has_bias) dev::bulk_g2s(smem + param_stride * (1u + has_beta), a.bias, row_bytes, &params_bar, pol_keep);
+    // one CTA per tile: take over the tiles of cancelled CTAs; else round-robin
+    const bool use_clc = EP_SLN_CLC && int64_t(gridDim.x) == ntiles;
+    dev::ClcStream clc(&clc_resp, &clc_bar);
+    if (use_clc) clc.request();  // the next tile is asked for while this CTA's own is copied
+    int64_t tile = blockIdx.x;
     dev::Ring ring(stages);
-    for (int64_t j = 0; j < mine; ++j, ring.next()) {
+    for (int64_t j = 0;; ++j, ring.next()) {
       const int st = ring.st;
       if (j >= stages && !dev::mbar_wait(&empty[st], ring.phase ^ 1u)) {
         // consumers stopped: wait (bounded) for the copies still in flight, then stop
         dev::mbar_wait(&params_bar, 0);
         for (int64_t k = j - stages; k < j; ++k)
           dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
+        clc.drain();
         return;
       }
-      const int64_t r0 = (blockIdx.x + j * gridDim.x) * RT;
+      tile_of[st] = tile;  // released to the consumers by the arrive below
+      if (tile < 0) {
+        dev::mbar_arrive(&full[st]);
+        break;
+      }
+      const int64_t r0 = tile * RT;
       const uint32_t nr = static_cast<uint32_t>(min(int64_t(RT), a.rows - r0));
       unsigned char* dst = stage0 + size_t(st) * stage_bytes;
       dev::mbar_arrive_expect_tx(&full[st], 2u * nr * row_bytes);
@@ -306,7 +325,14 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
           if (++sr == a.skip_rows) sr = 0;
         }
       }
+      if (use_clc) {
+        tile = clc.next();
+      } else {
+        tile += gridDim.x;
+        if (tile >= ntiles) tile = -1;
+      }
     }
+    clc.drain();
     return;
   }
 
@@ -323,14 +349,16 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
   bool ok = dev::mbar_wait(&params_bar, 0);
 
   dev::Ring ring(stages);
-  for (int64_t i = 0; i < mine; ++i, ring.next()) {
+  for (;; ring.next()) {
     const int st = ring.st;
     ok = dev::mbar_wait(&full[st], ring.phase) && ok;
     if constexpr (TPR > 32) ok = dev::named_barrier_and(bar_id, TPR, ok);
     else ok = __all_sync(0xffffffffu, ok);
     if (!ok) return;
+    const int64_t tile = tile_of[st];  // the same for every consumer
+    if (tile < 0) return;
 
-    const int64_t r = (blockIdx.x + i * gridDim.x) * RT + g;
+    const int64_t r = tile * RT + g;
     const bool active = r < a.rows;
     const unsigned char* stage = stage0 + size_t(st) * stage_bytes;
     const T* s_in = reinterpret_cast<const T*>(stage) + g * H;
@@ -511,7 +539,9 @@ cudaError_t launch_t(const SlnArgs& a, int sm_count, cudaStream_t stream, int* l
         cudaError_t e = resident_ctas(reinterpret_cast<const void*>(f), kWsThreads, smem, &per_sm);
         if (e != cudaSuccess) return e;
         const int64_t ntiles = (a.rows + rt - 1) / rt;
-        const unsigned grid = static_cast<unsigned>(std::min<int64_t>(ntiles, int64_t(sm_count) * per_sm));
+        // one CTA per tile under launch control, else a persistent grid
+        const bool clc = EP_SLN_CLC && ntiles <= int64_t(INT32_MAX);
+        const unsigned grid = static_cast<unsigned>(clc ? ntiles : std::min<int64_t>(ntiles, int64_t(sm_count) * per_sm));
         f<<<grid, kWsThreads, smem, stream>>>(k, stages, ntiles, param_stride);
         *launches += 1;
         return cudaGetLastError();

@@ -166,6 +166,80 @@ struct Ring {
   }
 };
 
+// ---------------------------------------------------------------------------
+// Dynamic work distribution with cluster launch control (sm_100+).  A kernel
+// launched with one CTA per work unit lets each running CTA ask the hardware
+// to cancel a CTA of the same grid that has not started yet and take over its
+// unit, so SMs that run faster take more units and the grid ends together.
+// The 16-byte answer lands in shared memory and completes `bar` with 16
+// transaction bytes; after a refusal (no CTA left to cancel) the CTA must not
+// ask again.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void clc_try_cancel(void* resp, uint64_t* bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+      ::"r"(smem_addr(resp)), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Decodes an answer (16-byte aligned): true, and the x index of the cancelled
+// CTA, if a CTA was cancelled.
+__device__ __forceinline__ bool clc_query(const void* resp, uint32_t* ctaid_x) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 r, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "mov.u32 %1, 0;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+      : "=r"(ok), "=r"(x)
+      : "r"(smem_addr(resp))
+      : "memory");
+  *ctaid_x = x;
+  return ok != 0;
+}
+
+// Orders this thread's earlier shared-memory accesses before later async-proxy
+// (bulk copy, launch control) writes to the same addresses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// One thread's stream of work units: this CTA's own unit, then those of the
+// CTAs it cancels, with one request kept in flight.  `resp` (16-byte aligned)
+// and `bar` (initialised with count 1) are the CTA's.
+struct ClcStream {
+  void* resp;
+  uint64_t* bar;
+  uint32_t phase = 0;
+  bool pending = false;  // a request is in flight
+  __device__ __forceinline__ ClcStream(void* r, uint64_t* b) : resp(r), bar(b) {}
+  __device__ __forceinline__ void request() {
+    mbar_arrive_expect_tx(bar, 16);
+    clc_try_cancel(resp, bar);
+    pending = true;
+  }
+  // The next unit, or -1 when no CTA is left to cancel (or the answer did not
+  // come within the bounded wait, which is counted as a timeout).
+  __device__ __forceinline__ int64_t next() {
+    if (!pending) return -1;
+    if (!mbar_wait(bar, phase)) return -1;  // still pending: drain() waits again
+    pending = false;
+    phase ^= 1u;
+    uint32_t x;
+    if (!clc_query(resp, &x)) return -1;
+    fence_proxy_async_smem();  // the answer is read before the next request overwrites it
+    request();
+    return int64_t(x);
+  }
+  // Before the CTA exits: wait (bounded) for a request still in flight.
+  __device__ __forceinline__ void drain() {
+    if (pending && mbar_wait(bar, phase)) pending = false;
+  }
+};
+
 // 16-byte shared-memory load.
 __device__ __forceinline__ uint4 lds16(const void* p) {
   return *reinterpret_cast<const uint4*>(p);

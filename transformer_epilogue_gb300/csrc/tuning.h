@@ -24,6 +24,11 @@
 #ifndef EP_SLN_TMA
 #define EP_SLN_TMA 1
 #endif
+// 1: one CTA per tile, running CTAs take over the tiles of CTAs they cancel
+// (cluster launch control); 0: persistent grid, tiles round-robin.
+#ifndef EP_SLN_CLC
+#define EP_SLN_CLC 1
+#endif
 
 // BiasSoftmax row kernel: the same four, plus the smallest threads-per-row
 // the staged kernel may use.
@@ -38,6 +43,10 @@
 #endif
 #ifndef EP_SM_TMA
 #define EP_SM_TMA 1
+#endif
+// 1: one CTA per tile with cluster launch control; 0: persistent round-robin.
+#ifndef EP_SM_CLC
+#define EP_SM_CLC 1
 #endif
 #ifndef EP_SM_TMA_MIN_TPR
 #define EP_SM_TMA_MIN_TPR 16
@@ -62,4 +71,8 @@
 #endif
 #ifndef EP_EW_TMA_MIN_CTAS
 #define EP_EW_TMA_MIN_CTAS 1
+#endif
+// 1: one CTA per tile with cluster launch control; 0: persistent round-robin.
+#ifndef EP_EW_CLC
+#define EP_EW_CLC 1
 #endif
