@@ -36,7 +36,7 @@
 #define EP_SM_TMA_TILE_BYTES 16384
 #endif
 #ifndef EP_SM_TMA_STAGE_BUDGET
-#define EP_SM_TMA_STAGE_BUDGET (100 * 1024)
+#define EP_SM_TMA_STAGE_BUDGET (64 * 1024)
 #endif
 #ifndef EP_SM_TMA_MIN_CTAS
 #define EP_SM_TMA_MIN_CTAS 1
