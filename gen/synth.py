@@ -118,6 +118,15 @@ def quick_gelu_inputs(numel, dtype="f32", seed=0, std=3.0):
     return dict(X=normal(g, (int(numel),), std).to(T), alpha=DEFAULT_ALPHA)
 
 
+def float32_bit_patterns(n: int, seed: int = 0) -> torch.Tensor:
+    """n float32 values with uniformly random bit patterns, the non-finite ones
+    dropped: every exponent (subnormals included) and both signs."""
+    g = _gen(seed)
+    bits = torch.randint(-(1 << 31), 1 << 31, (n,), generator=g, dtype=torch.int64).to(torch.int32)
+    x = bits.view(torch.float32)
+    return x[torch.isfinite(x)].contiguous()
+
+
 # --------------------------------------------------------------------------
 # named workloads: the transformer-activation shapes the ops are measured on
 # --------------------------------------------------------------------------

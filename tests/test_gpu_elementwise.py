@@ -107,6 +107,15 @@ def test_quick_gelu_f32_wide_range(lib, alpha):
     assert_elementwise_close(out, oracle.quick_gelu(x, alpha), torch.float32)
 
 
+@pytest.mark.parametrize("alpha", [1.702, -0.5])
+def test_quick_gelu_f32_random_bits(lib, alpha):
+    # random float32 bit patterns: every exponent, subnormal inputs, products
+    # alpha*x that overflow, results that underflow
+    x = synth.float32_bit_patterns(1 << 21, seed=11)
+    out = run_gelu(lib, x, alpha)
+    assert_elementwise_close(out, oracle.quick_gelu(x, alpha), torch.float32)
+
+
 def test_quick_gelu_f16_all_values(lib):
     # every finite float16 value
     bits = torch.arange(0, 1 << 16, dtype=torch.int32).to(torch.int16)

@@ -81,29 +81,45 @@ k_bias_add(const T* x, const T* __restrict__ bias, const T* skip, T* y, int64_t 
   }
 }
 
-// x * sigmoid(alpha x), float32 result within a few ulp (relative).
-//  z = alpha*x is split into z + zlo exactly (FMA), and exp(z + zlo) is taken
-//  as exp(z)*(1 + zlo), which removes the error of rounding alpha*x.
-//  z >= 0 : x / (1 + e^{-z});   -64 < z < 0 : x * t/(1 + t), t = e^{z};
-//  z <= -64: 1/(1+e^z) rounds to 1, and x*e^z is formed as (x*e^{z+64})*e^{-64}
-//  so that no intermediate leaves the normal range before the last product.
+// x * sigmoid(alpha x), float32 result within a few ulp (relative), with the
+// hardware 2^x and reciprocal instead of a library exponential and a divide.
+//  * w = -|alpha x| is carried as wh + wl, exact (TwoProduct: the rounding
+//    error of a product is one FMA away, Dekker / Ogita-Rump-Oishi), and so
+//    is p = wh log2(e) = ph + pl, with log2(e) itself split into a float and
+//    its remainder.
+//  * u = e^{w} = 2^{ph} * e^{pl ln2 + wl} ~ 2^{ph} (1 + c), c = pl ln2 + wl:
+//    |c| < 2^-16, so the dropped c^2/2 is far below a float32 ulp.
+//  * z >= 0: y = x / (1 + u);  z < 0: y = x u / (1 + u);  1 + u is in [1, 2],
+//    so the approximate reciprocal stays in the normal range.
+//  * For ph < -100, 1 + u rounds to 1: z >= 0 gives y = x; z < 0 gives
+//    y = (x 2^{ph + 64} (1 + c)) 2^-64 (2^{ph} itself would leave the normal
+//    range below -126), one last product into the subnormal range; below
+//    ph = -200, |y| < 2^-180 and rounds to (signed) zero.
 __device__ __forceinline__ float quick_gelu_f32(float x, float alpha) {
-  const float z = __fmul_rn(alpha, x);
-  float zlo = fmaf(alpha, x, -z);
-  if (!isfinite(zlo)) zlo = 0.f;
-  if (z >= 0.f) {
-    float u = expf(-z);
-    u = fmaf(-u, zlo, u);
-    return __fdiv_rn(x, __fadd_rn(1.0f, u));
+  constexpr float kL = 1.44269502162933349609375f;  // log2(e) rounded to float32
+  constexpr float kLlo = 1.92596298909109e-08f;     // log2(e) - kL
+  constexpr float kLn2 = 0.6931471805599453f;
+  const float zh = __fmul_rn(alpha, x);
+  float zl = fmaf(alpha, x, -zh);
+  if (!isfinite(zl)) zl = 0.f;  // alpha x overflowed (or x is not finite)
+  const bool pos = zh >= 0.f;
+  const float wh = pos ? -zh : zh;
+  const float wl = pos ? -zl : zl;
+  const float ph = __fmul_rn(wh, kL);
+  if (!(ph >= -200.f)) return pos ? x : __fmul_rn(x, 0.f);  // also ph = NaN: x is NaN
+  const float pl = fmaf(wh, kLlo, fmaf(wh, kL, -ph));
+  const float c = fmaf(pl, kLn2, wl);
+  if (ph >= -100.f) {
+    float u = dev::ex2_approx(ph);
+    u = fmaf(u, c, u);
+    const float r = dev::rcp_approx(__fadd_rn(1.0f, u));
+    return pos ? __fmul_rn(x, r) : __fmul_rn(__fmul_rn(x, u), r);
   }
-  if (z > -64.f) {
-    float t = expf(z);
-    t = fmaf(t, zlo, t);
-    return __fmul_rn(x, __fdiv_rn(t, __fadd_rn(1.0f, t)));
-  }
-  float t = expf(__fadd_rn(z, 64.0f));
-  t = fmaf(t, zlo, t);
-  return __fmul_rn(__fmul_rn(x, t), 1.60381089e-28f /* e^-64 */);
+  // u < 2^-100: 1 / (1 + u) rounds to 1
+  if (pos) return x;
+  float u = dev::ex2_approx(__fadd_rn(ph, 64.0f));
+  u = fmaf(u, c, u);
+  return __fmul_rn(__fmul_rn(x, u), 5.42101086242752217e-20f /* 2^-64 */);
 }
 
 // float16 results: float32 arithmetic with the fast exponential and divide;

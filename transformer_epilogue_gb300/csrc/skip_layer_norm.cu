@@ -456,9 +456,8 @@ using KernelFn = void (*)(SlnKernelArgs);
 // Row-group shapes (threads per row TPR, fragments per thread NV) compiled for
 // each (T, VW), in order of capacity TPR*NV*VW; the first that holds the row is
 // taken.  Every shape keeps at most 32 floats of the row per thread, so the row
-// stays in registers without spilling; the largest holds kRowMax elements.
+// stays in registers without spilling; the largest holds 16384 elements.
 // Longer rows use the three-pass kernel.
-constexpr int64_t kRowMax = 16384;
 
 template <typename T, int VW>
 KernelFn pick_kernel(int64_t H, int* tpr_out) {
