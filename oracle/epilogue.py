@@ -234,19 +234,38 @@ def bias_softmax(data, bias, axis=DEFAULT_AXIS, is_inner_broadcast=0, rows=None)
 # BiasAdd
 # ---------------------------------------------------------------------------
 
+def _two_sum(a, b):
+    """Knuth's TwoSum in float64: s = fl(a + b) and its rounding error e, so
+    that a + b = s + e exactly (no overflow for the operand types here)."""
+    s = a + b
+    bb = s - a
+    e = (a - (s - bb)) + (b - bb)
+    return s, e
+
+
 def bias_add(X, bias, skip):
-    """Y = X + bias[c] + skip over (N, S, C), in float64.
+    """Y = X + bias[c] + skip over (N, S, C): the exact sum, rounded to float64.
 
     com.microsoft.BiasAdd manifest, `description` and `inputs`: bias is
     broadcast over the channel (last) dimension, then the residual is added.
-    The float64 sum of T-typed (fp16 or fp32) terms is exact for fp16 and
-    within one float64 rounding for fp32.
+    A plain float64 sum is exact for fp16 terms but not for fp32 or bf16 ones
+    whose exponents differ by more than 53 bits, and where the skip then
+    cancels a term only that rounding error is left.  So the sum is formed as
+    an error-free expansion (TwoSum twice): x + b = s1 + e1 and
+    s1 + skip = s2 + e2 exactly; y = s2 + (e1 + e2) is within two float64
+    roundings of the exact sum, cancellation or not.  Non-finite sums are the
+    plain float64 ones.
     """
     x = _np(X).astype(np.float64)
     b = _np(bias).astype(np.float64)
     s = _np(skip).astype(np.float64)
     C = x.shape[-1]
-    return (x + b.reshape((1,) * (x.ndim - 1) + (C,))) + s
+    b = np.broadcast_to(b.reshape((1,) * (x.ndim - 1) + (C,)), x.shape)
+    with np.errstate(invalid="ignore"):
+        s1, e1 = _two_sum(x, b)
+        s2, e2 = _two_sum(s1, s)
+        y = s2 + (e1 + e2)
+    return np.where(np.isfinite(s2), y, s2)
 
 
 # ---------------------------------------------------------------------------

@@ -37,10 +37,11 @@ MUTANTS = [
     ("softmax_no_max_shift", "e = np.exp(z - m[:, None])", "e = np.exp(z)"),
     ("softmax_bias_dropped", "z = d2[r].astype(np.float64) + b2[br].astype(np.float64)", "z = d2[r].astype(np.float64)"),
     ("softmax_global_sum", "out[pos] = e / np.sum(e, axis=1)[:, None]", "out[pos] = e / np.sum(e)"),
-    ("bias_add_bias_reversed", "(x + b.reshape((1,) * (x.ndim - 1) + (C,))) + s",
-     "(x + b[::-1].reshape((1,) * (x.ndim - 1) + (C,))) + s"),
-    ("bias_add_skip_dropped", "(x + b.reshape((1,) * (x.ndim - 1) + (C,))) + s",
-     "(x + b.reshape((1,) * (x.ndim - 1) + (C,)))"),
+    ("bias_add_bias_reversed", "b = np.broadcast_to(b.reshape((1,) * (x.ndim - 1) + (C,)), x.shape)",
+     "b = np.broadcast_to(b[::-1].reshape((1,) * (x.ndim - 1) + (C,)), x.shape)"),
+    ("bias_add_skip_dropped", "s2, e2 = _two_sum(s1, s)", "s2, e2 = _two_sum(s1, 0.0 * s)"),
+    ("bias_add_uncompensated", "        y = s2 + (e1 + e2)\n", "        y = s2\n"),
+    ("bias_add_two_sum_error", "    e = (a - (s - bb)) + (b - bb)\n", "    e = b - bb\n"),
     ("gelu_sign", "sig[pos] = 1.0 / (1.0 + np.exp(-t[pos]))", "sig[pos] = 1.0 / (1.0 + np.exp(t[pos]))"),
     ("gelu_alpha_not_float32", "a = float(np.float32(alpha))", "a = float(alpha)"),
     ("gelu_stable_branch", "sig[~pos] = et / (1.0 + et)", "sig[~pos] = et"),

@@ -347,6 +347,38 @@ def test_bias_add_exact_rational_brute_force(dtype):
                     assert abs(got - exact) <= abs(exact) * Fraction(1, 2 ** 52) + Fraction(1, 2 ** 200)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("mode", ["skip_is_minus_x", "skip_is_minus_bias", "random"])
+def test_bias_add_exact_with_wide_exponents(dtype, mode):
+    # terms whose exponents differ by more than float64's 53 bits, with a skip
+    # that cancels one of them: the result is still the exact sum to within
+    # two float64 roundings (a plain float64 sum would keep only the rounding
+    # error of x + bias)
+    g = np.random.default_rng(17)
+
+    def wide(*shape):
+        v = (g.random(shape) + 1.0) * np.exp2(g.integers(-60, 61, shape)) * np.where(g.random(shape) < 0.5, -1, 1)
+        t = torch.from_numpy(v.astype(np.float32))
+        return t.to(torch.bfloat16) if dtype == "bf16" else t
+
+    x = wide(2, 3, 8)
+    b = wide(8)
+    if mode == "skip_is_minus_x":
+        s = -x
+    elif mode == "skip_is_minus_bias":
+        s = (-b).expand(2, 3, 8).contiguous()
+    else:
+        s = wide(2, 3, 8)
+    out = oracle.bias_add(x, b, s)
+    xf, bf, sf = (t.double().numpy() for t in (x, b, s))
+    for n in range(2):
+        for t in range(3):
+            for c in range(8):
+                exact = Fraction(float(xf[n, t, c])) + Fraction(float(bf[c])) + Fraction(float(sf[n, t, c]))
+                got = Fraction(float(out[n, t, c]))
+                assert abs(got - exact) <= abs(exact) * Fraction(1, 2 ** 51), (n, t, c, float(got), float(exact))
+
+
 # ---------------------------------------------------------------------------
 # QuickGelu
 # ---------------------------------------------------------------------------
