@@ -92,3 +92,28 @@ def test_bias_add_bf16_cancellation(lib):
     s = (-(x.double() + b.double()) + torch.randn(4, 8, 64, generator=g).double() * 1e-2).to(torch.bfloat16)
     out = ew.run_bias_add(lib, dict(X=x, bias=b, skip=s))
     assert_elementwise_close(out, oracle.bias_add(x, b, s), torch.bfloat16)
+
+
+@pytest.mark.parametrize("mode", ["skip_is_minus_x", "skip_is_minus_bias", "random"])
+def test_bias_add_bf16_wide_exponents(lib, mode):
+    # terms whose exponents differ by far more than float32's 24 bits, so that
+    # x + bias is not exact in float32, and a skip that cancels one of them:
+    # the result must still be within a bfloat16 spacing of the exact sum
+    g = torch.Generator().manual_seed(5)
+
+    def wide(*shape):
+        m = torch.rand(*shape, generator=g) + 1.0
+        e = torch.randint(-60, 61, shape, generator=g).double()
+        sign = torch.where(torch.rand(*shape, generator=g) < 0.5, -1.0, 1.0)
+        return (sign * m * torch.pow(2.0, e)).to(torch.bfloat16)
+
+    x = wide(4, 64, 64)
+    b = wide(64)
+    if mode == "skip_is_minus_x":
+        s = -x
+    elif mode == "skip_is_minus_bias":
+        s = (-b).expand(4, 64, 64).contiguous()
+    else:
+        s = wide(4, 64, 64)
+    out = ew.run_bias_add(lib, dict(X=x, bias=b, skip=s))
+    assert_elementwise_close(out, oracle.bias_add(x, b, s), torch.bfloat16)

@@ -81,6 +81,31 @@ def test_bias_add_in_place(lib):
     assert_elementwise_close(x.cpu(), oracle.bias_add(d["X"], d["bias"], d["skip"]), torch.float16)
 
 
+@pytest.mark.parametrize("mode", ["skip_is_minus_x", "skip_is_minus_bias", "random"])
+def test_bias_add_f32_wide_exponents(lib, mode):
+    # terms whose exponents differ by far more than float32's 24 bits, with a
+    # skip that cancels one of them: the result must be within the float32
+    # tolerance of the exact sum
+    g = torch.Generator().manual_seed(9)
+
+    def wide(*shape):
+        m = torch.rand(*shape, generator=g) + 1.0
+        e = torch.randint(-60, 61, shape, generator=g).float()
+        sign = torch.where(torch.rand(*shape, generator=g) < 0.5, -1.0, 1.0)
+        return sign * m * torch.pow(2.0, e)
+
+    x = wide(4, 64, 64)
+    b = wide(64)
+    if mode == "skip_is_minus_x":
+        s = -x
+    elif mode == "skip_is_minus_bias":
+        s = (-b).expand(4, 64, 64).contiguous()
+    else:
+        s = wide(4, 64, 64)
+    out = run_bias_add(lib, dict(X=x, bias=b, skip=s))
+    assert_elementwise_close(out, oracle.bias_add(x, b, s), torch.float32)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 7, 8, 9, 15, 16, 17, 1000, 4099, 1 << 20, (1 << 20) + 5])
 def test_quick_gelu_sizes(lib, dtype, n):

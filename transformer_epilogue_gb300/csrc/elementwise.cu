@@ -42,12 +42,26 @@ __device__ __forceinline__ float two_sum3(float a, float b, float c) {
   return __fadd_rn(s2, __fadd_rn(e1, e2));
 }
 
+// (a + b) + c for bfloat16 results: the rounding error e of a + b (Knuth's
+// TwoSum) is added after c.  Where a + b and c cancel, their sum is exact
+// (Sterbenz) and e is added with one rounding; elsewhere |(a + b) + c| is at
+// least about half of |a + b| and e is below its float32 ulp.  Either way the
+// float32 result is within two float32 ulp of the exact sum, far inside a
+// bfloat16 ulp.
+__device__ __forceinline__ float sum3_bf16(float a, float b, float c) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return __fadd_rn(__fadd_rn(s, c), e);
+}
+
 template <typename T>
 __device__ __forceinline__ float bias_add_elem(float x, float b, float s) {
   // float16 terms span at most 40 bits, so the float32 sum is within a float16
-  // ulp without compensation; float32 and bfloat16 (float32's exponent range)
-  // take the compensated sum.
+  // ulp without compensation; bfloat16 (float32's exponent range) compensates
+  // the first addition, float32 both.
   if constexpr (std::is_same_v<T, __half>) return __fadd_rn(__fadd_rn(x, b), s);
+  else if constexpr (std::is_same_v<T, __nv_bfloat16>) return sum3_bf16(x, b, s);
   else return two_sum3(x, b, s);
 }
 
@@ -129,11 +143,24 @@ __device__ __forceinline__ float quick_gelu_f16(float x, float alpha) {
   return __fdividef(x, 1.0f + u);
 }
 
-// float16 results use the fast form; float32 and bfloat16 (whose range reaches
-// results far below the fast form's flush-to-zero threshold) the accurate one.
+// bfloat16 results: float32 arithmetic with the hardware 2^x and reciprocal,
+// t = -alpha x log2(e) rounded once; the errors (a few float32 ulp, and
+// |t| 2^-24 from rounding t) are far below a bfloat16 ulp.  bfloat16 keeps
+// float32's exponent range, down to 2^-133, but the hardware 2^x flushes
+// results below 2^-126: where e^{alpha x} < 2^-64, 1 + e^{alpha x} rounds to 1
+// and x e^{alpha x} is formed as (x 2^{64 - t}) 2^-64.  nal2e = -alpha log2(e).
+__device__ __forceinline__ float quick_gelu_bf16(float x, float nal2e) {
+  const float t = __fmul_rn(x, nal2e);
+  if (t > 64.f) return __fmul_rn(__fmul_rn(x, dev::ex2_approx(__fsub_rn(64.f, t))), 5.42101086242752217e-20f);
+  return __fmul_rn(x, dev::rcp_approx(__fadd_rn(1.0f, dev::ex2_approx(t))));
+}
+
+// float16 results use the fast form, bfloat16 the fast form with its
+// underflow branch, float32 the accurate one.
 template <typename T>
 __device__ __forceinline__ float quick_gelu_elem(float x, float alpha) {
   if constexpr (std::is_same_v<T, __half>) return quick_gelu_f16(x, alpha);
+  else if constexpr (std::is_same_v<T, __nv_bfloat16>) return quick_gelu_bf16(x, -alpha * dev::kLog2e);
   else return quick_gelu_f32(x, alpha);
 }
 
@@ -288,7 +315,8 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
       const float xv = dev::ld1_stream(x + e);
       float yv;
       if constexpr (BIAS_ADD) yv = bias_add_elem<T>(xv, dev::ld1_keep(bias + e % C), dev::ld1_stream(skip + e));
-      else if constexpr (!std::is_same_v<T, __half>) yv = quick_gelu_f32(xv, alpha);
+      else if constexpr (std::is_same_v<T, float>) yv = quick_gelu_f32(xv, alpha);
+      else if constexpr (std::is_same_v<T, __nv_bfloat16>) yv = quick_gelu_bf16(xv, nal2e);
       else yv = quick_gelu_fast(xv, nal2e);
       dev::st1_stream(y + e, yv);
     }
@@ -334,9 +362,12 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
           dev::lds_unpack(reinterpret_cast<const T*>(smem) + c, b);
 #pragma unroll
           for (int e = 0; e < VW; ++e) a[u][e] = bias_add_elem<T>(a[u][e], b[e], sk[u][e]);
-        } else if constexpr (!std::is_same_v<T, __half>) {
+        } else if constexpr (std::is_same_v<T, float>) {
 #pragma unroll
           for (int e = 0; e < VW; ++e) a[u][e] = quick_gelu_f32(a[u][e], alpha);
+        } else if constexpr (std::is_same_v<T, __nv_bfloat16>) {
+#pragma unroll
+          for (int e = 0; e < VW; ++e) a[u][e] = quick_gelu_bf16(a[u][e], nal2e);
         } else {
 #pragma unroll
           for (int e = 0; e < VW; ++e) a[u][e] = quick_gelu_fast(a[u][e], nal2e);
