@@ -7,6 +7,10 @@ f32 (2,128,768); BiasSoftmax f16 (32,16,512,512) causal, f32 64x262144 and
 
 value        = minimum bytes of all ops (every input read once, every output
                written once, reused vectors counted once) / device time of a step
+               (the timed steps carry one event pair, around the dominant op;
+               each event record costs ~2 us of stream time)
+ops          = per-op means from a separate loop with an event pair around
+               every op
 e2e          = the same metric with each step's inputs copied host->device from
                pinned memory and outputs copied back, inside the timed region
 roofline     = the dominant kernel's algorithmic bytes / its mean CUDA-event
@@ -45,6 +49,8 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 
 # Step order: each small workload follows a large streaming one.
+K_BREAKDOWN = 50  # steps of the per-op breakdown loop
+
 ORDER = [
     "sln_f16_16384x4096_bias_residual",
     "sln_f32_2x128x768",
@@ -64,16 +70,16 @@ ORDER = [
 # step serves from L2, and writes still dirty in L2 at a kernel's end are not
 # counted.)
 NCU_TRAFFIC = {
-    "sln_f16_16384x4096_bias_residual": 478418688,
-    "sln_f32_2x128x768": 1608192,
-    "sln_f32_32x2048x1024_bcast_skip": 486072832,
-    "bias_add_f16_16x1024x4096": 348874496,
-    "bias_softmax_f32_64x262144_cyclic": 153454336,
-    "quick_gelu_f16_67108867": 206232832,
-    "bias_softmax_f16_32x16x512x512_causal": 492861184,
-    "bias_softmax_f32_8x1048576": 75627776,
+    "sln_f16_16384x4096_bias_residual": 478610176,
+    "sln_f32_2x128x768": 1610240,
+    "sln_f32_32x2048x1024_bcast_skip": 485596672,
+    "bias_add_f16_16x1024x4096": 348338176,
+    "bias_softmax_f32_64x262144_cyclic": 153264128,
+    "quick_gelu_f16_67108867": 206700288,
+    "bias_softmax_f16_32x16x512x512_causal": 492539136,
+    "bias_softmax_f32_8x1048576": 75611904,
 }
-NCU_TRAFFIC_SOURCE_HASH = "26a2566be6acee17"
+NCU_TRAFFIC_SOURCE_HASH = "bdaab2c7994596d7"
 
 
 def kernel_source_hash() -> str:
@@ -412,10 +418,26 @@ def main(argv=None):
             w.call()
     torch.cuda.synchronize()
 
-    # timed region: K steps, per-op events on the launching stream
-    K = args.steps
+    # per-op breakdown (its own loop, before the timed region): an event pair
+    # around every op; each event record adds ~2 us of stream time, so these
+    # loops are not the step time
+    B = max(5, min(K_BREAKDOWN, args.steps))
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in work]
-          for _ in range(K)]
+          for _ in range(B)]
+    torch.cuda.synchronize()
+    for k in range(B):
+        for i, w in enumerate(work):
+            ev[k][i][0].record(stream)
+            w.call()
+            ev[k][i][1].record(stream)
+    torch.cuda.synchronize()
+    per_op_ms = [statistics.fmean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(B)) for i in range(len(work))]
+    dom = max(range(len(ORDER)), key=lambda i: per_op_ms[i])
+
+    # timed region: K steps; one event pair per step around the dominant op
+    # (its launch duration for the roofline), no other per-op events
+    K = args.steps
+    dom_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -428,9 +450,12 @@ def main(argv=None):
     t_start.record(stream)
     for k in range(K):
         for i, w in enumerate(work):
-            ev[k][i][0].record(stream)
-            w.call()
-            ev[k][i][1].record(stream)
+            if i == dom:
+                dom_ev[k][0].record(stream)
+                w.call()
+                dom_ev[k][1].record(stream)
+            else:
+                w.call()
     t_end.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -438,7 +463,7 @@ def main(argv=None):
     launches = te.kernel_launch_count() - n_launch0
     clk = clocks.stop(wall0, wall1)
     total_ms = t_start.elapsed_time(t_end)
-    per_op_ms = [statistics.fmean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(K)) for i in range(len(work))]
+    dom_ms = statistics.fmean(a.elapsed_time(b) for a, b in dom_ev)
 
     # e2e: pinned host inputs -> device, op, outputs -> pinned host, per step
     pinned_in = [{k: hosts[n][k].pin_memory() for k in w.inputs} for n, w in zip(ORDER, work)]
@@ -511,9 +536,8 @@ def main(argv=None):
         if r:
             o["rows_per_s"] = r / (ms / 1e3)
         ops[n] = o
-    dom = max(range(len(ORDER)), key=lambda i: per_op_ms[i])
     dom_name = ORDER[dom]
-    achieved = bytes_per[dom] / (per_op_ms[dom] / 1e3) / 1e9
+    achieved = bytes_per[dom] / (dom_ms / 1e3) / 1e9
     src_hash = kernel_source_hash()
     traffic = NCU_TRAFFIC.get(dom_name) if NCU_TRAFFIC_SOURCE_HASH == src_hash else None
     line = {
@@ -525,8 +549,11 @@ def main(argv=None):
                    "streams buffers disjoint from the previous op's)", "parallelism": f"replicas x{ws}"},
         "frac_of_measured_peak": value / peak,
         "ops": ops,
+        "ops_timing": f"separate loop of {B} steps, an event pair around every op (each record adds ~2 us)",
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src},
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
+                     "duration_us": dom_ms * 1e3,
+                     "duration_source": "event pair around the op in every timed step, mean"},
         "e2e": {"value": e2e_units / (e2e_ms / 1e3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                 "pipeline": "uploads, kernels and downloads on three streams, overlapped across ops"},
