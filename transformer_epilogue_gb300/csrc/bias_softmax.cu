@@ -56,6 +56,8 @@ __device__ __forceinline__ int64_t bias_row(const SmKernelArgs& a, int64_t r) {
 template <typename T, int VW, int TPR, int NV>
 __global__ void __launch_bounds__(TPR > 256 ? TPR : 256)
 k_bias_softmax_rows(const SmKernelArgs a) {
+  dev::pdl_wait();
+  dev::pdl_trigger();
   constexpr int BS = TPR > 256 ? TPR : 256;
   constexpr int RPC = BS / TPR;
   __shared__ float red_a[BS / 32];
@@ -140,6 +142,8 @@ constexpr int kPackedMax = 8;
 
 template <typename T>
 __global__ void __launch_bounds__(256) k_bias_softmax_packed(const SmKernelArgs a) {
+  dev::pdl_wait();
+  dev::pdl_trigger();
   const T* data = static_cast<const T*>(a.data);
   const T* __restrict__ bias = static_cast<const T*>(a.bias);
   T* out = static_cast<T*>(a.output);
@@ -237,6 +241,8 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
     dev::mbar_init_fence();
   }
   __syncthreads();
+  dev::pdl_wait();
+  dev::pdl_trigger();
   if (int64_t(blockIdx.x) >= ntiles) return;
 
   if (tid >= kWsConsumers) {
@@ -427,6 +433,8 @@ __device__ __forceinline__ void load_chunk(const SmKernelArgs& a, int64_t r, int
 template <typename T, int VW>
 __global__ void __launch_bounds__(kSplitThreads)
 k_softmax_chunk_stats(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t nchunks, float2* stats) {
+  dev::pdl_wait();
+  dev::pdl_trigger();
   __shared__ float red_a[kSplitThreads / 32];
   __shared__ float red_b[kSplitThreads / 32];
   const int64_t total = nrows * nchunks;
@@ -458,6 +466,8 @@ template <typename T, int VW>
 __global__ void __launch_bounds__(kSplitThreads)
 k_softmax_chunk_normalize(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t nchunks,
                           const float2* stats) {
+  dev::pdl_wait();
+  dev::pdl_trigger();
   __shared__ float red_a[kSplitThreads / 32];
   __shared__ float red_b[kSplitThreads / 32];
   constexpr int NV = SplitNV<T, VW>::value;
@@ -611,8 +621,13 @@ k_softmax_split_tma(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t n
     dev::mbar_init_fence();
   }
   __syncthreads();
-  // pass 1 lets the (programmatically dependent) pass 2 be scheduled as its CTAs retire
-  if (STATS) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // pass 1 waits for the work before it, then lets the (programmatically
+  // dependent) pass 2 be scheduled as its CTAs retire; pass 2's producer waits
+  // for pass 1 below, before it reads the chunk statistics
+  if (STATS) {
+    dev::pdl_wait();
+    dev::pdl_trigger();
+  }
   if (mine <= 0) return;
 
   if (warp == kSpWarps) {
@@ -658,7 +673,8 @@ k_softmax_split_tma(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t n
     }
 
     // pass 2: the statistics come from pass 1, which may still be finishing
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    dev::pdl_wait();
+    dev::pdl_trigger();
     int64_t cur_row = -1;
     float2 cur = make_float2(0.f, 0.f);
     SplitCursor hc;  // the tile whose header is written next
@@ -869,7 +885,9 @@ cudaError_t launch_split(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_cou
         const int64_t total = nr * nchunks;
         const unsigned g1 = static_cast<unsigned>(std::min<int64_t>(total, int64_t(sm_count) * per1));
         const unsigned g2 = static_cast<unsigned>(std::min<int64_t>(total, int64_t(sm_count) * per2));
-        k_softmax_split_tma<T, true><<<g1, kSpThreads, smem, stream>>>(k, r0, nr, nchunks, stats, stages);
+        cudaError_t el = launch(k_softmax_split_tma<T, true>, dim3(g1), dim3(kSpThreads), smem, stream, k, r0, nr,
+                                nchunks, stats, stages);
+        if (el != cudaSuccess) return el;
         // pass 2 may start while pass 1 drains; it waits for pass 1 (griddepcontrol.wait)
         // before reading the chunk statistics, and reads only data before that
         cudaLaunchConfig_t cfg = {};
@@ -895,11 +913,13 @@ cudaError_t launch_split(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_cou
   for (int64_t r0 = 0; r0 < a.rows; r0 += win) {
     const int64_t nr = std::min(win, a.rows - r0);
     const unsigned grid = static_cast<unsigned>(std::min(nr * nchunks, cap));
-    k_softmax_chunk_stats<T, VW><<<grid, kSplitThreads, 0, stream>>>(k, r0, nr, nchunks, stats);
-    k_softmax_chunk_normalize<T, VW><<<grid, kSplitThreads, 0, stream>>>(k, r0, nr, nchunks, stats);
-    *launches += 2;
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch(k_softmax_chunk_stats<T, VW>, dim3(grid), dim3(kSplitThreads), 0, stream, k, r0, nr,
+                           nchunks, stats);
+    if (e == cudaSuccess)
+      e = launch(k_softmax_chunk_normalize<T, VW>, dim3(grid), dim3(kSplitThreads), 0, stream, k, r0, nr, nchunks,
+                 static_cast<const float2*>(stats));
     if (e != cudaSuccess) return e;
+    *launches += 2;
   }
   return cudaSuccess;
 }
@@ -955,9 +975,8 @@ bool launch_tma_rows(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_count, 
   // one CTA per tile under launch control, else a persistent grid
   const bool clc = EP_SM_CLC && ntiles <= int64_t(INT32_MAX);
   const unsigned grid = static_cast<unsigned>(clc ? ntiles : std::min<int64_t>(ntiles, int64_t(sm_count) * per_sm));
-  f<<<grid, kWsThreads, smem, stream>>>(k, stages, int(slots), ntiles);
-  *launches += 1;
-  *err = cudaGetLastError();
+  *err = launch(f, dim3(grid), dim3(kWsThreads), smem, stream, k, stages, int(slots), ntiles);
+  if (*err == cudaSuccess) *launches += 1;
   return true;
 }
 
@@ -969,7 +988,8 @@ cudaError_t launch_t(const SoftmaxArgs& a, int sm_count, int l2_bytes, cudaStrea
   if (a.cols <= kPackedMax) {
     const int64_t blocks = (a.rows + 255) / 256;
     const unsigned grid = static_cast<unsigned>(std::min<int64_t>(blocks, int64_t(sm_count) * 32));
-    k_bias_softmax_packed<T><<<grid, 256, 0, stream>>>(k);
+    cudaError_t el = launch(k_bias_softmax_packed<T>, dim3(grid), dim3(256), 0, stream, k);
+    if (el != cudaSuccess) return el;
     *launches += 1;
     return cudaGetLastError();
   }
@@ -984,7 +1004,8 @@ cudaError_t launch_t(const SoftmaxArgs& a, int sm_count, int l2_bytes, cudaStrea
     const int rpc = bs / tpr;
     const int64_t need = (a.rows + rpc - 1) / rpc;
     const int64_t cap = int64_t(sm_count) * 64 * (2048 / bs);
-    fn<<<static_cast<unsigned>(std::min(need, cap)), bs, 0, stream>>>(k);
+    cudaError_t el = launch(fn, dim3(static_cast<unsigned>(std::min(need, cap))), dim3(bs), 0, stream, k);
+    if (el != cudaSuccess) return el;
     *launches += 1;
     return cudaGetLastError();
   }

@@ -96,6 +96,15 @@ template <> struct Conv<__nv_bfloat16> {
   }
 };
 
+// Programmatic dependent launch.  pdl_wait returns once the grids this one
+// depends on have completed and their memory is visible (at once for a grid
+// launched without that dependency); every kernel calls it before its first
+// global memory access.  pdl_trigger, called after it, lets a dependent grid
+// launch once every CTA of this one has triggered or exited, so a dependent
+// never starts before this grid's own predecessors have completed.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // 2^x and 1/x with the hardware approximations (flush-to-zero): relative
 // errors of a few float32 ulp, used where the result is rounded to float16 or
 // must only meet an absolute tolerance.  e^x is taken as 2^(x * log2(e)).

@@ -69,6 +69,8 @@ __device__ __forceinline__ float bias_add_elem(float x, float b, float s) {
 template <typename T, int VW>
 __global__ void __launch_bounds__(kThreads)
 k_bias_add(const T* x, const T* __restrict__ bias, const T* skip, T* y, int64_t nfrag, int64_t C) {
+  dev::pdl_wait();
+  dev::pdl_trigger();
   const int64_t stride = int64_t(gridDim.x) * kThreads;
   const int64_t cfrag = C / VW;
   for (int64_t i0 = int64_t(blockIdx.x) * kThreads + threadIdx.x; i0 < nfrag; i0 += stride * kUnroll) {
@@ -169,6 +171,8 @@ __device__ __forceinline__ float quick_gelu_elem(float x, float alpha) {
 template <typename T, int VW>
 __global__ void __launch_bounds__(kThreads)
 k_quick_gelu(const T* x, T* y, int64_t head, int64_t nfrag, int64_t n, float alpha) {
+  dev::pdl_wait();
+  dev::pdl_trigger();
   const int64_t tid = int64_t(blockIdx.x) * kThreads + threadIdx.x;
   const int64_t stride = int64_t(gridDim.x) * kThreads;
   const T* xb = x + head;
@@ -259,6 +263,8 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
     dev::mbar_init_fence();
   }
   __syncthreads();
+  dev::pdl_wait();
+  dev::pdl_trigger();
   const bool have_tiles = int64_t(blockIdx.x) < ntiles;
 
   if (tid >= kEwConsumers) {
@@ -404,8 +410,8 @@ cudaError_t launch_ew_tma(const T* x, const T* skip, const T* bias, T* y, int64_
   const unsigned grid = static_cast<unsigned>(
       std::max<int64_t>(1, clc ? ntiles : std::min<int64_t>(ntiles, int64_t(sm_count) * per_sm)));
   const uint32_t step_frag = BIAS_ADD ? uint32_t((int64_t(kEwConsumers) * VW) % C) : 0u;
-  fn<<<grid, kEwThreads, smem, stream>>>(x, skip, bias, y, nfrag, n, C, alpha, stages, bias_bytes, step_frag);
-  return cudaGetLastError();
+  return launch(fn, dim3(grid), dim3(kEwThreads), smem, stream, x, skip, bias, y, nfrag, n, C, alpha, stages,
+                bias_bytes, step_frag);
 }
 
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -428,14 +434,15 @@ cudaError_t bias_add_t(const BiasAddArgs& a, int sm_count, cudaStream_t stream, 
     *launches += 1;
     return launch_ew_tma<T, true>(x, s, b, y, a.n, a.C, 0.f, sm_count, stream);
   }
+  cudaError_t e;
   if (a.C % VW == 0 && al16(x) && al16(b) && al16(s) && al16(y)) {
     const int64_t nfrag = a.n / VW;
-    k_bias_add<T, VW><<<grid_for(nfrag, sm_count), kThreads, 0, stream>>>(x, b, s, y, nfrag, a.C);
+    e = launch(k_bias_add<T, VW>, dim3(grid_for(nfrag, sm_count)), dim3(kThreads), 0, stream, x, b, s, y, nfrag, a.C);
   } else {
-    k_bias_add<T, 1><<<grid_for(a.n, sm_count), kThreads, 0, stream>>>(x, b, s, y, a.n, a.C);
+    e = launch(k_bias_add<T, 1>, dim3(grid_for(a.n, sm_count)), dim3(kThreads), 0, stream, x, b, s, y, a.n, a.C);
   }
-  *launches += 1;
-  return cudaGetLastError();
+  if (e == cudaSuccess) *launches += 1;
+  return e;
 }
 
 template <typename T>
@@ -449,16 +456,18 @@ cudaError_t quick_gelu_t(const QuickGeluArgs& a, int sm_count, cudaStream_t stre
     *launches += 1;
     return launch_ew_tma<T, false>(x, nullptr, nullptr, y, a.n, 1, a.alpha, sm_count, stream);
   }
+  cudaError_t e;
   if (ox == oy) {
     const int64_t head = std::min<int64_t>(a.n, int64_t((16 - ox) & 15u) / int64_t(sizeof(T)));
     const int64_t nfrag = (a.n - head) / VW;
-    k_quick_gelu<T, VW><<<grid_for(std::max<int64_t>(nfrag, VW), sm_count), kThreads, 0, stream>>>(
-        x, y, head, nfrag, a.n, a.alpha);
+    e = launch(k_quick_gelu<T, VW>, dim3(grid_for(std::max<int64_t>(nfrag, VW), sm_count)), dim3(kThreads), 0, stream,
+               x, y, head, nfrag, a.n, a.alpha);
   } else {
-    k_quick_gelu<T, 1><<<grid_for(a.n, sm_count), kThreads, 0, stream>>>(x, y, 0, a.n, a.n, a.alpha);
+    e = launch(k_quick_gelu<T, 1>, dim3(grid_for(a.n, sm_count)), dim3(kThreads), 0, stream, x, y, int64_t(0), a.n,
+               a.n, a.alpha);
   }
-  *launches += 1;
-  return cudaGetLastError();
+  if (e == cudaSuccess) *launches += 1;
+  return e;
 }
 
 }  // namespace

@@ -11,7 +11,29 @@
 
 #include <cuda_runtime.h>
 
+#include "tuning.h"
+
 namespace ep {
+
+// Launches `kernel` on `stream`, with EP_PDL as a programmatic dependent of the
+// work before it in the stream: its CTAs may be scheduled while that work
+// drains, and they wait for it (pdl_wait) before touching global memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          Args... args) {
+  static_assert(sizeof...(KArgs) == sizeof...(Args), "one argument per kernel parameter");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = EP_PDL ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Resident CTAs per SM of `fn` with `threads` threads and `smem` bytes of
 // dynamic shared memory on the current device (>= 1).

@@ -50,6 +50,8 @@ struct SlnKernelArgs {
 template <typename T, int VW, int TPR, int NV>
 __global__ void __launch_bounds__(TPR > 256 ? TPR : 256)
 k_skip_layer_norm(const SlnKernelArgs a) {
+  dev::pdl_wait();
+  dev::pdl_trigger();
   constexpr int BS = TPR > 256 ? TPR : 256;
   constexpr int RPC = BS / TPR;  // rows per CTA
   __shared__ float red_a[BS / 32];
@@ -164,6 +166,8 @@ k_skip_layer_norm(const SlnKernelArgs a) {
 // element by the thread that read it, so exact in-place aliasing stays valid.
 template <typename T>
 __global__ void __launch_bounds__(1024) k_skip_layer_norm_long(const SlnKernelArgs a) {
+  dev::pdl_wait();
+  dev::pdl_trigger();
   __shared__ float red_a[32];
   __shared__ float red_b[32];
   const T* in = static_cast<const T*>(a.input);
@@ -277,6 +281,8 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
     dev::mbar_init_fence();
   }
   __syncthreads();
+  dev::pdl_wait();
+  dev::pdl_trigger();
   if (int64_t(blockIdx.x) >= ntiles) return;
 
   if (tid >= kWsConsumers) {
@@ -541,9 +547,9 @@ cudaError_t launch_t(const SlnArgs& a, int sm_count, cudaStream_t stream, int* l
         // one CTA per tile under launch control, else a persistent grid
         const bool clc = EP_SLN_CLC && ntiles <= int64_t(INT32_MAX);
         const unsigned grid = static_cast<unsigned>(clc ? ntiles : std::min<int64_t>(ntiles, int64_t(sm_count) * per_sm));
-        f<<<grid, kWsThreads, smem, stream>>>(k, stages, ntiles, param_stride);
-        *launches += 1;
-        return cudaGetLastError();
+        e = launch(f, dim3(grid), dim3(kWsThreads), smem, stream, k, stages, ntiles, param_stride);
+        if (e == cudaSuccess) *launches += 1;
+        return e;
       }
     }
   }
@@ -555,14 +561,15 @@ cudaError_t launch_t(const SlnArgs& a, int sm_count, cudaStream_t stream, int* l
     const int64_t need = (a.rows + rpc - 1) / rpc;
     const int64_t cap = int64_t(sm_count) * 64 * (2048 / bs);  // many waves, then grid-stride
     const unsigned grid = static_cast<unsigned>(std::min(need, cap));
-    fn<<<grid, bs, 0, stream>>>(k);
-  } else {
-    const int64_t cap = int64_t(sm_count) * 2 * 16;
-    const unsigned grid = static_cast<unsigned>(std::min(a.rows, cap));
-    k_skip_layer_norm_long<T><<<grid, 1024, 0, stream>>>(k);
+    cudaError_t e = launch(fn, dim3(grid), dim3(bs), 0, stream, k);
+    if (e == cudaSuccess) *launches += 1;
+    return e;
   }
-  *launches += 1;
-  return cudaGetLastError();
+  const int64_t cap = int64_t(sm_count) * 2 * 16;
+  const unsigned grid = static_cast<unsigned>(std::min(a.rows, cap));
+  cudaError_t e = launch(k_skip_layer_norm_long<T>, dim3(grid), dim3(1024), 0, stream, k);
+  if (e == cudaSuccess) *launches += 1;
+  return e;
 }
 
 }  // namespace

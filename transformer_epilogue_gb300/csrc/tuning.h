@@ -9,6 +9,12 @@
 #define EP_MBAR_SUSPEND_NS 0
 #endif
 
+// 1: every kernel is launched as a programmatic dependent of the preceding
+// work in its stream (its launch and prologue overlap that work's tail).
+#ifndef EP_PDL
+#define EP_PDL 1
+#endif
+
 // SkipLayerNormalization: largest tile of rows per stage, shared memory for
 // one CTA's stages, minimum resident CTAs per SM the compiler must allow for
 // (register cap), and 0/1 to use the staged kernel at all.
