@@ -72,16 +72,16 @@ ORDER = [
 # step serves from L2, and writes still dirty in L2 at a kernel's end are not
 # counted.)
 NCU_TRAFFIC = {
-    "sln_f16_16384x4096_bias_residual": 478610176,
-    "sln_f32_2x128x768": 1610240,
-    "sln_f32_32x2048x1024_bcast_skip": 485596672,
-    "bias_add_f16_16x1024x4096": 348338176,
-    "bias_softmax_f32_64x262144_cyclic": 153264128,
-    "quick_gelu_f16_67108867": 206700288,
-    "bias_softmax_f16_32x16x512x512_causal": 492539136,
-    "bias_softmax_f32_8x1048576": 75611904,
+    "sln_f16_16384x4096_bias_residual": 478622720,
+    "sln_f32_2x128x768": 1607936,
+    "sln_f32_32x2048x1024_bcast_skip": 485809920,
+    "bias_add_f16_16x1024x4096": 349105408,
+    "bias_softmax_f32_64x262144_cyclic": 153185024,
+    "quick_gelu_f16_67108867": 206546432,
+    "bias_softmax_f16_32x16x512x512_causal": 492797696,
+    "bias_softmax_f32_8x1048576": 75609856,
 }
-NCU_TRAFFIC_SOURCE_HASH = "bdaab2c7994596d7"
+NCU_TRAFFIC_SOURCE_HASH = "a971cc8406ff1743"
 
 
 def kernel_source_hash() -> str:
