@@ -347,6 +347,33 @@ def build_hosts():
     return hosts
 
 
+def sliced_workload(name, batch):
+    """The named workload with its leading dimension cut to `batch`: every
+    tensor whose first dimension equals the data's is sliced (so a causal mask
+    follows its data and SkipLayerNorm's skip its input, while a broadcast skip
+    or a cyclic bias is kept whole)."""
+    d = synth.workload(name)
+    if not batch:
+        return d
+    lead = next(d[k] for k in ("input", "data", "X") if k in d).shape[0]
+    if batch > lead:
+        raise ValueError(f"batch {batch} > leading dimension {lead} of {name}")
+    return {k: (v[:batch].contiguous() if isinstance(v, torch.Tensor) and v.dim() and v.shape[0] == lead else v)
+            for k, v in d.items()}
+
+
+def run_profile(args):
+    """Runs one workload `--reps` times and nothing else (a target for ncu)."""
+    import transformer_epilogue_gb300 as te
+    te.load_library()
+    w = DeviceWorkload(args.profile, sliced_workload(args.profile, args.batch), torch.device("cuda"))
+    for _ in range(args.reps):
+        w.call()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": args.profile, "batch": args.batch, "reps": args.reps}), flush=True)
+    return 0
+
+
 def run_reference(args, ws, rank):
     """The reference arm: the float64 CPU oracle, as it stands, on bounded
     samples of the same workloads (rank 0 only)."""
@@ -390,8 +417,13 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=ORDER, help="run only this workload --reps times (for ncu)")
+    ap.add_argument("--batch", type=int, default=0, help="with --profile: cut the leading dimension to this")
+    ap.add_argument("--reps", type=int, default=3, help="with --profile: calls of the op")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
+    if args.profile:
+        return run_profile(args)
 
     ws, rank, local = dist_env()
     if ws > 1:
