@@ -205,6 +205,28 @@ def workload(name: str) -> dict:
     return d
 
 
+def device_normal(shape, dtype="f16", seed=0, std=1.0, device="cuda") -> torch.Tensor:
+    """N(0, std) draws made on the device with a seeded generator, 2^26 at a
+    time, then cast to T: for tensors too large to build on the host."""
+    T = DTYPES[dtype]
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    out = torch.empty(tuple(shape), dtype=T, device=device)
+    flat = out.view(-1)
+    step = 1 << 26
+    for i in range(0, flat.numel(), step):
+        n = min(step, flat.numel() - i)
+        flat[i:i + n] = (torch.randn(n, generator=g, device=device, dtype=torch.float32) * std).to(T)
+    return out
+
+
+def sample_indices(n: int, k: int, seed: int = 1234) -> set:
+    """About k distinct indices in [0, n), drawn without materialising a
+    permutation (n may be in the billions)."""
+    g = _gen(seed)
+    return set(torch.randint(0, n, (k,), generator=g, dtype=torch.int64).tolist())
+
+
 def sample_rows(n_rows: int, k: int, seed: int = 1234) -> list:
     """k distinct row indices in [0, n_rows), always including the first and last
     rows; used to check full-size outputs row by row against the oracle."""
