@@ -83,3 +83,48 @@ def test_split_softmax_after_producer(lib):
     z1 = torch.from_numpy(oracle.quick_gelu(q, 1.702)).float()
     assert_norm_close(y.cpu(), oracle.bias_softmax(z1, b, axis=1, is_inner_broadcast=0), torch.float32)
     assert_elementwise_close(z.cpu(), oracle.quick_gelu(q, -1.0), torch.float32)
+
+
+def test_two_streams_at_once(lib):
+    # two independent chains on two streams at the same time: the CTAs of both
+    # grids share the SMs and each grid hands out only its own tiles.  The
+    # kernels are deterministic, so the results must equal a sequential run's
+    # bit for bit.
+    R, H = 2048, 4096
+    ins = [synth.sln_inputs((R, H), dtype="f16", has_bias=True, seed=60 + k) for k in range(2)]
+    longs = [synth.bias_softmax_inputs((4, 1 << 18), (1, 1 << 18), "f32", data_std=2.0, seed=70 + k) for k in range(2)]
+
+    def setup(k):
+        d, lg = ins[k], longs[k]
+        t = {n: d[n].cuda() for n in ("input", "skip", "gamma", "beta", "bias")}
+        t["ld"], t["lb"] = lg["data"].cuda(), lg["bias"].cuda()
+        t["o1"], t["o2"], t["o3"] = _nan_like(t["input"]), _nan_like(t["input"]), _nan_like(t["ld"])
+        t["ws"] = torch.empty(lib.ep_bias_softmax_workspace_size(torch.float32, tuple(t["ld"].shape), 1),
+                              dtype=torch.uint8, device="cuda")
+        return t
+
+    def chain(t, eps):
+        for _ in range(4):
+            lib.ep_skip_layer_norm(t["input"], t["skip"], t["gamma"], t["beta"], t["bias"], eps, output=t["o1"])
+            lib.ep_quick_gelu(t["o1"], 1.702, Y=t["o2"])
+            lib.ep_bias_softmax(t["ld"], t["lb"], axis=1, is_inner_broadcast=0, output=t["o3"], workspace=t["ws"])
+            lib.ep_quick_gelu(t["o2"], 1.0, Y=t["o2"])                     # in place
+
+    conc = [setup(k) for k in range(2)]
+    seq = [setup(k) for k in range(2)]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    for k, st in enumerate(streams):
+        with torch.cuda.stream(st):
+            chain(conc[k], ins[k]["epsilon"])
+    torch.cuda.synchronize()
+    for k in range(2):
+        chain(seq[k], ins[k]["epsilon"])
+    torch.cuda.synchronize()
+    for k in range(2):
+        for n in ("o1", "o2", "o3"):
+            assert torch.equal(conc[k][n].view(torch.int16 if n != "o3" else torch.int32),
+                               seq[k][n].view(torch.int16 if n != "o3" else torch.int32)), (k, n)
+        d = ins[k]
+        assert_norm_close(conc[k]["o1"].cpu(), oracle.skip_layer_norm(d["input"], d["skip"], d["gamma"], d["beta"],
+                                                                      d["bias"], d["epsilon"])["output"], torch.float16)
