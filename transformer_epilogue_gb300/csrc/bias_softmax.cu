@@ -866,10 +866,10 @@ cudaError_t launch_split(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_cou
                          cudaStream_t stream, int* launches) {
   const int64_t nchunks = (a.cols + chunk_cols<T>() - 1) / chunk_cols<T>();
   float2* stats = static_cast<float2*>(a.workspace);
-  // rows per window: keep a window's data within 3/4 of L2 so that the second
-  // read (normalize) hits L2
+  // rows per window: keep a window's data within a fraction of L2 so that the
+  // second read (normalize) hits L2
   const int64_t row_bytes = a.cols * int64_t(sizeof(T));
-  const int64_t budget = std::max<int64_t>(int64_t(l2_bytes) * 3 / 4, 1);
+  const int64_t budget = std::max<int64_t>(int64_t(l2_bytes) * EP_SM_SPLIT_WINDOW_QUARTERS / 4, 1);
   const int64_t win = std::max<int64_t>(1, budget / row_bytes);
   if constexpr (VW > 1) {
     if (EP_SM_TMA) {

@@ -61,6 +61,11 @@
 // Split-row softmax (rows longer than the row kernels hold): bytes of data in
 // one stage (4096, 8192 or 16384; the stage also holds as many bytes of bias),
 // and shared memory for the stages of one CTA.
+// Rows of a window of the split-row pair: their data fills at most this many
+// quarters of L2.
+#ifndef EP_SM_SPLIT_WINDOW_QUARTERS
+#define EP_SM_SPLIT_WINDOW_QUARTERS 3
+#endif
 #ifndef EP_SM_SPLIT_TILE_BYTES
 #define EP_SM_SPLIT_TILE_BYTES 16384
 #endif
