@@ -8,20 +8,24 @@
 // workgroup per row) and `longrow_split` (block_stats -> row_stats ->
 // normalize, rows >= 65536) are the prior art for the two paths below.
 //
-// Row path (rows that fit on chip): a group of TPR threads owns a row; z is
-// kept in float32 registers, so data and output cross HBM once.  Max and sum
-// are warp-shuffle (+ shared memory) reductions.
+// Row path (rows of at most 16384 elements): a group of TPR threads owns a row;
+// z is kept in float32 registers, so data and output cross HBM once.  Max and
+// sum are warp-shuffle (+ named-barrier) reductions.  16-byte-aligned rows take
+// the staged kernel (k_bias_softmax_rows_tma), others the register kernel;
+// rows of at most 8 elements a thread-per-row kernel.
 //
-// Split-row path (longer rows): the row is cut into chunks of one CTA each.
-//   k_softmax_chunk_stats   : per chunk (m_b, s_b) = (max z, sum exp(z - m_b))
-//                             -> workspace
-//   k_softmax_chunk_normalize: every CTA first combines its row's chunk stats,
-//                             M = max m_b, S = sum s_b exp(m_b - M) (the
-//                             manifest's separate row_stats pass is folded in
-//                             here), then re-reads its chunk and writes
-//                             exp(z - M) / S.
+// Split-row path (longer rows): rows are cut into 16 KB chunks and a pair of
+// launches runs over them:
+//   pass 1: per chunk (or per CTA's part of a row) (m_b, s_b) =
+//           (max z, sum exp(z - m_b)) -> workspace
+//   pass 2: M = max m_b, S = sum s_b exp(m_b - M) per row (the manifest's
+//           separate row_stats pass is folded in here), then the chunk is
+//           read again and exp(z - M) / S written.
+// The staged pair (k_softmax_split_tma) serves 16-byte-aligned rows, the
+// register pair (k_softmax_chunk_stats / k_softmax_chunk_normalize) the rest.
 // The host runs the pair over windows of rows sized to stay resident in L2,
-// so the second read of a chunk is normally served from L2, not HBM.
+// so the second read of a chunk is normally served from L2, not HBM.  Every
+// launch is a programmatic dependent of the work before it in the stream.
 #include <algorithm>
 #include <climits>
 #include <atomic>
@@ -188,8 +192,8 @@ __global__ void __launch_bounds__(256) k_bias_softmax_packed(const SmKernelArgs 
 // Shared-memory-staged, warp-specialised row kernel (the fast path for
 // 16-byte-aligned rows).
 //
-// A persistent CTA has kWsConsumers consumer threads in row groups of TPR and
-// one producer warp.  Tiles are RT = kWsConsumers/TPR consecutive data rows.  A
+// A CTA has kWsConsumers consumer threads in row groups of TPR and one
+// producer warp.  Tiles are RT = kWsConsumers/TPR consecutive data rows.  A
 // stage holds the tile's data rows and, after them, only the distinct bias
 // rows those data rows use (at most `bias_slots`):
 //   inner broadcast: bias rows r0/ir .. (r0+nr-1)/ir, one contiguous copy;

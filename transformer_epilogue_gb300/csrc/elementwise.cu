@@ -4,14 +4,20 @@
 // Y = X + bias[c] + skip over (N, S, C)) and com.microsoft.QuickGelu manifest
 // (`description`, `attributes.alpha`: Y = X * sigmoid(alpha * X)).
 //
-// Design (GB300): a persistent grid (a whole number of CTAs per SM) strides
-// over 128-bit fragments; each thread loads U independent fragments of every
-// streamed operand before it uses any, so an SM keeps tens of KB of loads in
-// flight.  Streamed data is loaded/stored evict-first; bias is read through the
-// read-only path and stays in L1/L2.  The manifests' vec4 / vec4-tail / scalar
-// variants become one kernel per op: a vector body, plus a scalar head (to
-// reach 16-byte alignment) and a scalar tail.  Misaligned operands with
-// different offsets take the same kernel with VW = 1.
+// Design (GB300), two kernel families per op:
+//  * 16-byte-aligned operands (at least one tile): the shared-memory-staged,
+//    warp-specialised kernel (k_elementwise_tma): a producer warp bulk-copies
+//    16 KB tiles into a ring of shared-memory stages, eight consumer warps
+//    compute and store; one CTA per tile, running CTAs take over the tiles of
+//    CTAs they cancel (cluster launch control).
+//  * Anything else: register kernels whose grid strides over 128-bit
+//    fragments; each thread loads U independent fragments of every streamed
+//    operand before it uses any, so an SM keeps tens of KB of loads in flight.
+//    A vector body, plus a scalar head (to reach 16-byte alignment) and a
+//    scalar tail; misaligned operands with different offsets use VW = 1.
+// Streamed data is loaded/stored evict-first; bias stays in shared memory or
+// the read-only path.  Every launch is a programmatic dependent of the work
+// before it in the stream.
 #include <algorithm>
 #include <climits>
 #include <type_traits>

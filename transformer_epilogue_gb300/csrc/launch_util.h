@@ -1,7 +1,9 @@
-// Host helpers for launching the shared-memory-staged kernels: raise a
-// kernel's dynamic shared-memory limit to the device's opt-in maximum once per
-// (kernel, device), and size a persistent grid from the occupancy calculator,
-// with the answers cached.
+// Host helpers for launching the kernels: `launch` (every kernel, as a
+// programmatic dependent of the work before it in the stream), and for the
+// shared-memory-staged kernels `resident_ctas`, which raises a kernel's dynamic
+// shared-memory limit to the device's opt-in maximum once per (kernel, device)
+// and asks the occupancy calculator how many CTAs fit on an SM, with the
+// answers cached.
 #pragma once
 
 #include <algorithm>

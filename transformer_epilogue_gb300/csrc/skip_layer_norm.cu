@@ -8,13 +8,16 @@
 // Design (GB300): a row is owned by a group of TPR threads; each thread keeps
 // NV fragments of VW elements of s = (input + skip) + bias in float32 registers,
 // so input, skip and the outputs each cross HBM exactly once.  The mean and the
-// variance are two reductions over the registers (warp shuffles, then shared
-// memory across the warps of a group): a two-pass variance with no second
-// global read.  gamma/beta/bias and a broadcast skip are read through the
-// read-only path at normal L2 priority (they are reused by every row); the
-// streamed tensors use evict-first loads and stores.  Rows too long for the
-// register budget fall back to a CTA-per-row kernel that re-reads the row
-// (three passes) instead of holding it.
+// variance are two reductions over the registers (warp shuffles, then a named
+// barrier or shared memory across the warps of a group): a two-pass variance
+// with no second global read.  16-byte-aligned rows take the staged kernel
+// (k_skip_layer_norm_tma: rows bulk-copied into shared memory by a producer
+// warp, gamma/beta/bias held in shared memory, tiles handed out by cluster
+// launch control); other rows the register kernel, which reads gamma/beta/bias
+// and a broadcast skip through the read-only path; rows too long for the
+// register budget a CTA-per-row kernel that re-reads the row (three passes).
+// The streamed tensors use evict-first loads and stores, and every launch is a
+// programmatic dependent of the work before it in the stream.
 #include <algorithm>
 #include <climits>
 
