@@ -60,6 +60,21 @@ def test_bias_add_misaligned(lib, dtype, offs):
     assert_elementwise_close(out, oracle.bias_add(d["X"], d["bias"], d["skip"]), d["X"].dtype)
 
 
+@pytest.mark.parametrize("dtype,offs", [
+    ("f16", {"X": 2, "skip": 2, "Y": 2}), ("f16", {"X": 14, "skip": 14, "Y": 14, "bias": 6}),
+    ("f16", {"bias": 2}), ("f32", {"X": 4, "skip": 4, "Y": 4}), ("f32", {"X": 8, "skip": 8, "Y": 8, "bias": 12}),
+    ("bf16", {"X": 6, "skip": 6, "Y": 6}),
+])
+@pytest.mark.parametrize("shape", [(3, 700, 1024), (2, 999, 4104)])
+def test_bias_add_same_offset_staged(lib, dtype, offs, shape):
+    # X, skip and Y at the same offset within 16 bytes (the bias at any): the
+    # staged kernel takes the aligned body after a scalar head, with the bias
+    # staged rotated by the head; tiles, the ragged last tile and the tail
+    d = synth.bias_add_inputs(shape, dtype, seed=sum(shape) + sum(offs.values()))
+    out = run_bias_add(lib, d, offsets=offs)
+    assert_elementwise_close(out, oracle.bias_add(d["X"], d["bias"], d["skip"]), d["X"].dtype)
+
+
 def test_bias_add_f32_cancellation(lib):
     # skip = -(x + bias) + small: plain float32 (x + b) + s loses the small part;
     # the compensated sum keeps it to within relative 1e-6.

@@ -242,7 +242,7 @@ __device__ __forceinline__ float quick_gelu_fast(float x, float nal2e) {
 template <typename T, bool BIAS_ADD>
 __global__ void __launch_bounds__(kEwThreads, EP_EW_TMA_MIN_CTAS)
 k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag, int64_t n, int64_t C,
-                  float alpha, int stages, uint32_t bias_bytes, uint32_t col_step_frag) {
+                  float alpha, int stages, uint32_t bias_bytes, uint32_t col_step_frag, int head, int bias_rot) {
   constexpr int VW = dev::Vec16<T>::N;
   constexpr int NOPS = BIAS_ADD ? 2 : 1;
   constexpr uint32_t kTileBytes = kEwTileFrags * 16u;
@@ -258,6 +258,10 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
   unsigned char* stage0 = smem + bias_bytes;  // bias_bytes is a multiple of 128
   const uint32_t stage_bytes = NOPS * kTileBytes;
   const int64_t ntiles = (nfrag + kEwTileFrags - 1) / kEwTileFrags;
+  // the 16-byte-aligned body: elements [head, head + nfrag * VW)
+  const T* xb = x + head;
+  const T* skb = BIAS_ADD ? skip + head : nullptr;
+  T* yb = y + head;
 
   if (tid == 0) {
     for (int st = 0; st < stages; ++st) {
@@ -278,9 +282,11 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
     if (tid != kEwConsumers || !have_tiles) return;
     const uint64_t pol_stream = dev::policy_evict_first();
     if constexpr (BIAS_ADD) {
-      const uint32_t cb = uint32_t(C) * uint32_t(sizeof(T));
-      dev::mbar_arrive_expect_tx(&bias_bar, cb);
-      dev::bulk_g2s(smem, bias, cb, &bias_bar, dev::policy_evict_last());
+      if (!bias_rot) {  // else the consumers fill shared memory themselves
+        const uint32_t cb = uint32_t(C) * uint32_t(sizeof(T));
+        dev::mbar_arrive_expect_tx(&bias_bar, cb);
+        dev::bulk_g2s(smem, bias, cb, &bias_bar, dev::policy_evict_last());
+      }
     }
     // one CTA per tile: take over the tiles of cancelled CTAs; else round-robin
     const bool use_clc = EP_EW_CLC && int64_t(gridDim.x) == ntiles;
@@ -291,7 +297,9 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
     for (int64_t j = 0;; ++j, ring.next()) {
       const int st = ring.st;
       if (j >= stages && !dev::mbar_wait(&empty[st], ring.phase ^ 1u)) {
-        if constexpr (BIAS_ADD) dev::mbar_wait(&bias_bar, 0);
+        if constexpr (BIAS_ADD) {
+          if (!bias_rot) dev::mbar_wait(&bias_bar, 0);
+        }
         for (int64_t k = j - stages; k < j; ++k)
           dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
         clc.drain();
@@ -307,8 +315,8 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
       const uint32_t bytes = static_cast<uint32_t>(min(int64_t(kEwTileFrags), nfrag - f0)) * 16u;
       unsigned char* dst = stage0 + size_t(st) * stage_bytes;
       dev::mbar_arrive_expect_tx(&full[st], NOPS * bytes);
-      dev::bulk_g2s(dst, x + f0 * VW, bytes, &full[st], pol_stream);
-      if constexpr (BIAS_ADD) dev::bulk_g2s(dst + kTileBytes, skip + f0 * VW, bytes, &full[st], pol_stream);
+      dev::bulk_g2s(dst, xb + f0 * VW, bytes, &full[st], pol_stream);
+      if constexpr (BIAS_ADD) dev::bulk_g2s(dst + kTileBytes, skb + f0 * VW, bytes, &full[st], pol_stream);
       if (use_clc) {
         tile = clc.next();
       } else {
@@ -322,8 +330,10 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
 
   // ---- consumers ----
   const float nal2e = -alpha * dev::kLog2e;
-  if (blockIdx.x == 0) {  // scalar tail (elements past the last whole fragment)
-    for (int64_t e = nfrag * VW + tid; e < n; e += kEwConsumers) {
+  if (blockIdx.x == 0) {  // scalar head (before the aligned body) and tail (past its last fragment)
+    const int64_t tail0 = head + nfrag * VW;
+    for (int64_t k = tid; k < head + (n - tail0); k += kEwConsumers) {
+      const int64_t e = k < head ? k : tail0 + (k - head);
       const float xv = dev::ld1_stream(x + e);
       float yv;
       if constexpr (BIAS_ADD) yv = bias_add_elem<T>(xv, dev::ld1_keep(bias + e % C), dev::ld1_stream(skip + e));
@@ -335,7 +345,20 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
   }
   if (!have_tiles) return;
   bool ok = true;
-  if constexpr (BIAS_ADD) ok = dev::mbar_wait(&bias_bar, 0);
+  if constexpr (BIAS_ADD) {
+    if (bias_rot) {
+      // bias rotated by `head`, so that the body's fragments (which start at
+      // element head) read it at 16-byte boundaries: slot j = bias[(j + head) mod C]
+      T* sbias = reinterpret_cast<T*>(smem);
+      for (int64_t j = tid; j < C; j += kEwConsumers) {
+        const int64_t src = j + head < C ? j + head : j + head - C;
+        sbias[j] = bias[src];
+      }
+      dev::named_barrier_sync(1, kEwConsumers);
+    } else {
+      ok = dev::mbar_wait(&bias_bar, 0);
+    }
+  }
   const uint32_t Cu = static_cast<uint32_t>(C);
   dev::Ring ring(stages);
   for (;; ring.next()) {
@@ -384,7 +407,7 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
 #pragma unroll
           for (int e = 0; e < VW; ++e) a[u][e] = quick_gelu_fast(a[u][e], nal2e);
         }
-        dev::stg_pack_stream(y + (f0 + f) * VW, a[u]);
+        dev::stg_pack_stream(yb + (f0 + f) * VW, a[u]);
       }
       if constexpr (BIAS_ADD) {
         c += col_step_frag;
@@ -397,12 +420,15 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
 constexpr uint32_t kEwStageBudget = EP_EW_TMA_STAGE_BUDGET;
 constexpr int64_t kEwMaxBiasBytes = 64 * 1024;
 
+// `head` elements precede the 16-byte-aligned body (x, skip and y share their
+// offset within 16 bytes); `bias_rot`: BiasAdd's bias is staged rotated by
+// head (needed when head > 0 or the bias itself is not 16-byte aligned).
 template <typename T, bool BIAS_ADD>
 cudaError_t launch_ew_tma(const T* x, const T* skip, const T* bias, T* y, int64_t n, int64_t C, float alpha,
-                          int sm_count, cudaStream_t stream) {
+                          int sm_count, cudaStream_t stream, int head, bool bias_rot) {
   constexpr int VW = dev::Vec16<T>::N;
   auto fn = k_elementwise_tma<T, BIAS_ADD>;
-  const int64_t nfrag = n / VW;
+  const int64_t nfrag = (n - head) / VW;
   const uint32_t bias_bytes = BIAS_ADD ? uint32_t((C * int64_t(sizeof(T)) + 127) / 128 * 128) : 0u;
   const uint32_t stage_bytes = (BIAS_ADD ? 2u : 1u) * kEwTileFrags * 16u;
   const int stages = std::min<int>(kEwMaxStages, std::max<int>(2, kEwStageBudget / stage_bytes));
@@ -417,7 +443,7 @@ cudaError_t launch_ew_tma(const T* x, const T* skip, const T* bias, T* y, int64_
       std::max<int64_t>(1, clc ? ntiles : std::min<int64_t>(ntiles, int64_t(sm_count) * per_sm)));
   const uint32_t step_frag = BIAS_ADD ? uint32_t((int64_t(kEwConsumers) * VW) % C) : 0u;
   return launch(fn, dim3(grid), dim3(kEwThreads), smem, stream, x, skip, bias, y, nfrag, n, C, alpha, stages,
-                bias_bytes, step_frag);
+                bias_bytes, step_frag, head, int(bias_rot));
 }
 
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -435,10 +461,15 @@ cudaError_t bias_add_t(const BiasAddArgs& a, int sm_count, cudaStream_t stream, 
   const T* b = static_cast<const T*>(a.bias);
   const T* s = static_cast<const T*>(a.skip);
   T* y = static_cast<T*>(a.y);
-  if (EP_EW_TMA && a.C % VW == 0 && al16(x) && al16(b) && al16(s) && al16(y) &&
-      a.C * int64_t(sizeof(T)) <= kEwMaxBiasBytes && a.n / VW >= kEwTileFrags) {
+  // X, skip and Y at the same offset within 16 bytes: a scalar head, then an
+  // aligned body for the staged kernel (the bias may have any alignment)
+  const uintptr_t ox = reinterpret_cast<uintptr_t>(x) & 15u;
+  const bool same = ox == (reinterpret_cast<uintptr_t>(s) & 15u) && ox == (reinterpret_cast<uintptr_t>(y) & 15u);
+  const int64_t head = same ? std::min<int64_t>(a.n, int64_t((16 - ox) & 15u) / int64_t(sizeof(T))) : 0;
+  if (EP_EW_TMA && same && a.C % VW == 0 && a.C * int64_t(sizeof(T)) <= kEwMaxBiasBytes &&
+      (a.n - head) / VW >= kEwTileFrags) {
     *launches += 1;
-    return launch_ew_tma<T, true>(x, s, b, y, a.n, a.C, 0.f, sm_count, stream);
+    return launch_ew_tma<T, true>(x, s, b, y, a.n, a.C, 0.f, sm_count, stream, int(head), head != 0 || !al16(b));
   }
   cudaError_t e;
   if (a.C % VW == 0 && al16(x) && al16(b) && al16(s) && al16(y)) {
@@ -458,9 +489,12 @@ cudaError_t quick_gelu_t(const QuickGeluArgs& a, int sm_count, cudaStream_t stre
   T* y = static_cast<T*>(a.y);
   const uintptr_t ox = reinterpret_cast<uintptr_t>(x) & 15u;
   const uintptr_t oy = reinterpret_cast<uintptr_t>(y) & 15u;
-  if (EP_EW_TMA && ox == 0 && oy == 0 && a.n / VW >= kEwTileFrags) {
-    *launches += 1;
-    return launch_ew_tma<T, false>(x, nullptr, nullptr, y, a.n, 1, a.alpha, sm_count, stream);
+  if (EP_EW_TMA && ox == oy) {  // same offset within 16 bytes: a scalar head, then the aligned body
+    const int64_t head = std::min<int64_t>(a.n, int64_t((16 - ox) & 15u) / int64_t(sizeof(T)));
+    if ((a.n - head) / VW >= kEwTileFrags) {
+      *launches += 1;
+      return launch_ew_tma<T, false>(x, nullptr, nullptr, y, a.n, 1, a.alpha, sm_count, stream, int(head), false);
+    }
   }
   cudaError_t e;
   if (ox == oy) {
