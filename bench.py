@@ -72,16 +72,16 @@ ORDER = [
 # step serves from L2, and writes still dirty in L2 at a kernel's end are not
 # counted.)
 NCU_TRAFFIC = {
-    "sln_f16_16384x4096_bias_residual": 478622720,
-    "sln_f32_2x128x768": 1607936,
-    "sln_f32_32x2048x1024_bcast_skip": 485809920,
-    "bias_add_f16_16x1024x4096": 349105408,
-    "bias_softmax_f32_64x262144_cyclic": 153185024,
-    "quick_gelu_f16_67108867": 206546432,
-    "bias_softmax_f16_32x16x512x512_causal": 492797696,
-    "bias_softmax_f32_8x1048576": 75609856,
+    "sln_f16_16384x4096_bias_residual": 478301696,
+    "sln_f32_2x128x768": 1609472,
+    "sln_f32_32x2048x1024_bcast_skip": 485484544,
+    "bias_add_f16_16x1024x4096": 347740416,
+    "bias_softmax_f32_64x262144_cyclic": 153245440,
+    "quick_gelu_f16_67108867": 206802688,
+    "bias_softmax_f16_32x16x512x512_causal": 492735744,
+    "bias_softmax_f32_8x1048576": 75604480,
 }
-NCU_TRAFFIC_SOURCE_HASH = "a971cc8406ff1743"
+NCU_TRAFFIC_SOURCE_HASH = "31120aa700e245b9"
 
 
 def kernel_source_hash() -> str:
@@ -415,7 +415,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=ORDER, help="run only this workload --reps times (for ncu)")
     ap.add_argument("--batch", type=int, default=0, help="with --profile: cut the leading dimension to this")
