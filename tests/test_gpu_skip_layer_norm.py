@@ -203,10 +203,14 @@ def test_workload_full_size_sampled_rows(lib, name):
     R = d["input"].numel() // H
     rows = synth.sample_rows(R, 512)
     check(d, out, s, rows=rows)
-    # properties at every row: before gamma/beta... not available; check the
-    # output is finite everywhere and the residual (when written) matches on
-    # a second, disjoint sample
+    # properties at every row: n = (y - beta) / gamma has mean 0 and mean
+    # square var / (var + eps) ~ 1 (up to the output rounding, averaged over H);
+    # a wrong, missing or misplaced row anywhere breaks them
     assert torch.isfinite(out).all()
+    y = out.reshape(R, H).double()
+    n = (y - (d["beta"].double() if d["beta"] is not None else 0.0)) / d["gamma"].double()
+    assert float(n.mean(dim=1).abs().max()) < 5e-4
+    assert float((n.pow(2).mean(dim=1) - 1.0).abs().max()) < 5e-3
     if s is not None:
         rows2 = synth.sample_rows(R, 512, seed=99)
         want = oracle.skip_bias_sum(d["input"], d["skip"], d["bias"], rows=rows2)
