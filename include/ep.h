@@ -18,6 +18,13 @@
  *  - Every call is asynchronous: it validates on the host, enqueues its kernel(s)
  *    on `stream` and returns without synchronising.  Outputs are valid once the
  *    stream reaches that point.  A NULL stream is the legacy default stream.
+ *  - Kernels are launched as programmatic dependents of the work before them in
+ *    the stream (CUDA programmatic dependent launch): their blocks may be
+ *    scheduled while that work drains, but no block reads or writes global
+ *    memory before every kernel ahead of it in the stream has completed, so the
+ *    ordering seen by the caller is ordinary stream order.  Calls may be
+ *    captured into CUDA graphs (the split-row workspace must then outlive the
+ *    graph).
  *  - All validation happens before anything is enqueued.  A contract violation
  *    returns EP_ERR_INVALID_ARG, a legal op this library does not implement
  *    (another element type, an unsupported rank) returns EP_ERR_UNSUPPORTED, a
@@ -29,8 +36,9 @@
  *  - Empty tensors (numel 0) return EP_OK without launching anything; their
  *    pointers may be NULL.
  *  - Pointers must be aligned to sizeof(T).  16-byte alignment is not
- *    required: it selects the 128-bit vector path, and other alignments take a
- *    scalar path with the same results.
+ *    required: it selects the 128-bit vector path (BiasAdd and QuickGelu also
+ *    when X, skip and Y share one offset within 16 bytes), and other alignments
+ *    take a scalar path with the same results.
  *  - An output may alias an input exactly (same address, same size: in place).
  *    Any other overlap between an output and another operand is rejected.
  *  - Counts and offsets are 64-bit.
