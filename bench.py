@@ -290,6 +290,19 @@ def calibrate(hosts, target_s, frac=1.0 / 8192):
     return frac, b, t
 
 
+def host_cpu() -> str:
+    """The host CPU's model name (lscpu), else the machine type."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
+
+
 def cpu_baseline(hosts, budget_s=15.0):
     old = pin_one_core()
     try:
@@ -297,7 +310,7 @@ def cpu_baseline(hosts, budget_s=15.0):
     finally:
         if old is not None:
             os.sched_setaffinity(0, old)
-    return {"value": b / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": b / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle", "host_cpu": host_cpu(),
             "sample": f"first {frac:.5f} of the rows of every workload (numpy float64, 1 pinned core), "
                       f"{b / 1e6:.1f} MB of minimum traffic in {t:.1f} s; host has {os.cpu_count()} cores"}
 
@@ -402,7 +415,7 @@ def run_reference(args, ws, rank):
             "data": "synthetic (seeded; gen/synth.py)",
             "config": {"workload": "all eight epilogue workloads (bounded row samples on the CPU)",
                        "sample_fraction_of_rows": frac},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "host_cpu": host_cpu(),
                              "sample": f"first {frac:.6f} of the rows of every workload per step"},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
