@@ -185,6 +185,43 @@ def test_workload_long_rows_full(lib, name, inner):
 # with all bias rows in one tile, and outer maps that wrap inside a tile)
 # ---------------------------------------------------------------------------
 
+# every row shape of the staged kernel: a group of TPR threads holds NV
+# 16-byte fragments of a row.  Exact shapes (cols = TPR*NV*VW) and ragged ones
+# (the last fragment column partly idle), several tiles of 256/TPR rows with a
+# partial last tile, bias broadcast both ways; and the sub-warp register shapes
+# (rows of 1 to 16 fragments held by 4 to 16 threads) over several CTAs.
+_EXACT_SHAPES = [(t, nv) for nv in (4, 5, 6, 7) for t in (16, 32, 64, 128, 256)] + [(256, 8), (16, 3), (16, 2)]
+_RAGGED_NFRAG = [40, 100, 200, 300, 700, 1500]   # 16x4, 32x4, 64x4, 128x4, 256x4, 256x8 with idle lanes
+
+
+def _shape_cases():
+    out = []
+    for dt, vw in (("f32", 4), ("f16", 8), ("bf16", 8)):
+        out += [(dt, t * nv * vw) for t, nv in _EXACT_SHAPES]
+        out += [(dt, nf * vw) for nf in _RAGGED_NFRAG]
+    return out
+
+
+@pytest.mark.parametrize("dtype,cols", _shape_cases())
+def test_staged_row_shapes(lib, dtype, cols):
+    rows, bias_rows = (115, 5) if cols <= 4096 else (40, 5)   # >= 7 tiles of up to 16 rows; >= 20 of 1 or 2
+    d = synth.bias_softmax_inputs((rows, cols), (bias_rows, cols), dtype, data_std=3.0, seed=cols)
+    for inner in (0, 1):
+        out = run(lib, d["data"], d["bias"], 1, inner)
+        check(d["data"], d["bias"], 1, inner, out)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("nfrag", [2, 3, 4, 5, 8, 9, 16])
+def test_subwarp_register_shapes(lib, dtype, nfrag):
+    cols = nfrag * (4 if dtype == "f32" else 8)
+    rows, bias_rows = 64 * 5 + 16, 4               # several CTAs of 64, 32 or 16 rows
+    d = synth.bias_softmax_inputs((rows, cols), (bias_rows, cols), dtype, data_std=3.0, seed=nfrag)
+    for inner in (0, 1):
+        out = run(lib, d["data"], d["bias"], 1, inner)
+        check(d["data"], d["bias"], 1, inner, out)
+
+
 @pytest.mark.parametrize("dtype,rows,cols,bias_rows,inner", [
     ("f16", 80003, 512, 11429, 1), ("f16", 80003, 512, 11429, 0), ("f16", 80003, 512, 7, 0),
     ("f16", 80003, 512, 7, 1), ("f32", 40000, 256, 40000, 0), ("f32", 30000, 1024, 3, 1),

@@ -238,6 +238,44 @@ def test_staged_many_tiles(lib, dtype, H, rows, skip_rows):
 
 
 # ---------------------------------------------------------------------------
+# every row shape of the staged kernel: a group of TPR threads holds NV
+# 16-byte fragments of a row.  Exact shapes (H = TPR*NV*VW) and ragged ones
+# (the last fragment column partly idle), each over several tiles of 256/TPR
+# rows with a partial last tile; and the sub-warp register shapes (a row of
+# 1 to 16 fragments held by 4 to 16 threads) over several CTAs.
+# ---------------------------------------------------------------------------
+
+_EXACT_SHAPES = [(t, nv) for nv in (3, 4, 5, 7) for t in (16, 32, 64, 128, 256)] + [(256, 6), (256, 8), (16, 2)]
+_RAGGED_NFRAG = [40, 100, 200, 300, 700, 1500]   # 16x4, 32x4, 64x4, 128x4, 256x4, 256x8 with idle lanes
+
+
+def _shape_cases():
+    out = []
+    for dt, vw in (("f32", 4), ("f16", 8), ("bf16", 8)):
+        out += [(dt, t * nv * vw) for t, nv in _EXACT_SHAPES]
+        out += [(dt, nf * vw) for nf in _RAGGED_NFRAG]
+    return out
+
+
+@pytest.mark.parametrize("dtype,H", _shape_cases())
+def test_staged_row_shapes(lib, dtype, H):
+    rows = 115 if H <= 4096 else 37                # >= 7 tiles of up to 16 rows; >= 19 tiles of 1 or 2 rows
+    d = synth.sln_inputs((rows, H), None, dtype, has_beta=True, has_bias=True, seed=H + rows)
+    out, s = run(lib, d, residual=True)
+    check(d, out, s)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("nfrag", [1, 2, 3, 4, 5, 8, 9, 16])
+def test_subwarp_register_shapes(lib, dtype, nfrag):
+    H = nfrag * (4 if dtype == "f32" else 8)
+    rows = 64 * 5 + 17                             # several CTAs of 64, 32 or 16 rows
+    d = synth.sln_inputs((rows, H), None, dtype, has_beta=True, has_bias=True, seed=nfrag)
+    out, s = run(lib, d, residual=True)
+    check(d, out, s)
+
+
+# ---------------------------------------------------------------------------
 # ep_skip_layer_norm_ex: the RMS (simplified) form and the per-row statistics
 # ---------------------------------------------------------------------------
 

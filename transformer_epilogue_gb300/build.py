@@ -49,6 +49,8 @@ def _compile(src: str, force: bool, verbose: bool, extra: list, build_dir: str =
     if not force and os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(path), _headers_mtime()):
         return obj
     cmd = [nvcc(), "-c", path, "-o", obj] + ARCH + COMMON + extra
+    if src.endswith(".cu"):  # the three kernel files compile side by side; each splits its optimizer over cores
+        cmd += ["-split-compile", str(max(1, (os.cpu_count() or 3) // 3))]
     if verbose:
         print(" ".join(cmd), flush=True)
     p = subprocess.run(cmd, capture_output=True, text=True)

@@ -844,9 +844,11 @@ RowFn pick_row_kernel(int64_t cols, int* tpr_out) {
     return k_bias_softmax_rows<T, VW, TPR_, NV_>;    \
   }
   if constexpr (VW == 8) {
+    EP_SM_CASE(4, 1) EP_SM_CASE(8, 1) EP_SM_CASE(16, 1)
     EP_SM_CASE(32, 1) EP_SM_CASE(32, 2) EP_SM_CASE(32, 4) EP_SM_CASE(64, 4)
     EP_SM_CASE(128, 4) EP_SM_CASE(256, 4) EP_SM_CASE(512, 4)
   } else if constexpr (VW == 4) {
+    EP_SM_CASE(4, 1) EP_SM_CASE(8, 1) EP_SM_CASE(16, 1)
     EP_SM_CASE(32, 1) EP_SM_CASE(32, 2) EP_SM_CASE(32, 4) EP_SM_CASE(32, 8)
     EP_SM_CASE(64, 8) EP_SM_CASE(128, 8) EP_SM_CASE(256, 8) EP_SM_CASE(512, 8)
   } else {
@@ -932,28 +934,59 @@ using TmaRowFn = void (*)(SmKernelArgs, int, int, int64_t);
 constexpr uint32_t kTmaTileBytes = EP_SM_TMA_TILE_BYTES;
 constexpr uint32_t kTmaStageBudget = EP_SM_TMA_STAGE_BUDGET;
 
-// Same shape rule as the staged SkipLayerNorm kernel: the first TPR whose
-// NV <= 8 fragments hold the row and whose RT-row data tile is <= 16 KB.
+// Row shapes: a row of nfrag = cols/VW 16-byte fragments is split over TPR
+// threads (a power of two, 16 to 256) holding NV fragments each; a tile is
+// RT = 256/TPR rows.  Measured on GB300 (128 MB of data, row lengths 256 to
+// 16384, bias broadcast either way), a shape that covers the row exactly beats
+// a ragged one by 10 to 30 %, and among exact shapes NV = 4 to 6 is best
+// (NV = 3 loses up to 5 %: the stage also carries bias rows, so fewer, fuller
+// threads per row pay off).  So the exact shape with the smallest NV >= 4,
+// then NV = 3, then NV = 2; rows with no exact shape take the first TPR whose
+// NV <= 8 fragments hold the row and whose data tile is at most kTmaTileBytes.
+inline int exact_tpr(int64_t nfrag, int nv) {
+  if (nfrag % nv != 0) return 0;
+  const int64_t t = nfrag / nv;
+  return (t >= 16 && t <= 256 && (t & (t - 1)) == 0) ? static_cast<int>(t) : 0;
+}
+
 template <typename T>
 TmaRowFn pick_tma_row_kernel(int64_t cols, int* rows_per_tile) {
   constexpr int VW = dev::Vec16<T>::N;
   const int64_t nfrag = cols / VW;
   const int64_t row_bytes = cols * int64_t(sizeof(T));
   if (nfrag < 32) return nullptr;
-  const int tprs[] = {16, 32, 64, 128, 256};
-  for (int tpr : tprs) {
+  // exact shapes; the compiled set is every (TPR, NV) this search can return
+  for (int nv : {4, 5, 6, 7, 8, 3, 2}) {
+    const int tpr = exact_tpr(nfrag, nv);
+    if (tpr == 0 || tpr < EP_SM_TMA_MIN_TPR) continue;
+    *rows_per_tile = kWsConsumers / tpr;
+#define EP_SM_TMA_EXACT(TPR_, NV_) \
+    if (tpr == TPR_ && nv == NV_) return k_bias_softmax_rows_tma<T, TPR_, NV_, true>;
+    EP_SM_TMA_EXACT(16, 4) EP_SM_TMA_EXACT(32, 4) EP_SM_TMA_EXACT(64, 4) EP_SM_TMA_EXACT(128, 4)
+    EP_SM_TMA_EXACT(256, 4)
+    EP_SM_TMA_EXACT(16, 5) EP_SM_TMA_EXACT(32, 5) EP_SM_TMA_EXACT(64, 5) EP_SM_TMA_EXACT(128, 5)
+    EP_SM_TMA_EXACT(256, 5)
+    EP_SM_TMA_EXACT(16, 6) EP_SM_TMA_EXACT(32, 6) EP_SM_TMA_EXACT(64, 6) EP_SM_TMA_EXACT(128, 6)
+    EP_SM_TMA_EXACT(256, 6)
+    EP_SM_TMA_EXACT(16, 7) EP_SM_TMA_EXACT(32, 7) EP_SM_TMA_EXACT(64, 7) EP_SM_TMA_EXACT(128, 7)
+    EP_SM_TMA_EXACT(256, 7)
+    EP_SM_TMA_EXACT(256, 8)   // NV = 8 below TPR = 256 is NV = 4 at twice the TPR
+    EP_SM_TMA_EXACT(16, 3)    // NV = 3 above TPR = 16 is NV = 6 at half the TPR
+    EP_SM_TMA_EXACT(16, 2)    // NV = 2 is reached only for nfrag = 32
+#undef EP_SM_TMA_EXACT
+    return nullptr;
+  }
+  for (int tpr : {16, 32, 64, 128, 256}) {
     const int64_t nv = (nfrag + tpr - 1) / tpr;
     if (nv > 8 || tpr < EP_SM_TMA_MIN_TPR) continue;
     const int rt = kWsConsumers / tpr;
     if (rt * row_bytes > kTmaTileBytes && tpr != 256) continue;
     *rows_per_tile = rt;
-#define EP_SM_TMA_CASE(TPR_, NV_)                                                 \
-  if (tpr == TPR_ && nv <= NV_)                                                   \
-    return nfrag == int64_t(TPR_) * NV_ ? k_bias_softmax_rows_tma<T, TPR_, NV_, true> \
-                                        : k_bias_softmax_rows_tma<T, TPR_, NV_, false>;
-    EP_SM_TMA_CASE(16, 2) EP_SM_TMA_CASE(16, 4) EP_SM_TMA_CASE(32, 4) EP_SM_TMA_CASE(64, 4) EP_SM_TMA_CASE(128, 4)
-    EP_SM_TMA_CASE(256, 4) EP_SM_TMA_CASE(256, 8)
-#undef EP_SM_TMA_CASE
+#define EP_SM_TMA_RAGGED(TPR_, NV_) \
+    if (tpr == TPR_ && nv <= NV_) return k_bias_softmax_rows_tma<T, TPR_, NV_, false>;
+    EP_SM_TMA_RAGGED(16, 4) EP_SM_TMA_RAGGED(32, 4) EP_SM_TMA_RAGGED(64, 4) EP_SM_TMA_RAGGED(128, 4)
+    EP_SM_TMA_RAGGED(256, 4) EP_SM_TMA_RAGGED(256, 8)
+#undef EP_SM_TMA_RAGGED
     return nullptr;
   }
   return nullptr;

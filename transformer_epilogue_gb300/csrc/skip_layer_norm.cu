@@ -477,9 +477,11 @@ KernelFn pick_kernel(int64_t H, int* tpr_out) {
     return k_skip_layer_norm<T, VW, TPR_, NV_>;         \
   }
   if constexpr (VW == 8) {
+    EP_SLN_CASE(4, 1) EP_SLN_CASE(8, 1) EP_SLN_CASE(16, 1)
     EP_SLN_CASE(32, 1) EP_SLN_CASE(32, 2) EP_SLN_CASE(32, 4) EP_SLN_CASE(64, 4)
     EP_SLN_CASE(128, 4) EP_SLN_CASE(256, 4) EP_SLN_CASE(512, 4)
   } else if constexpr (VW == 4) {
+    EP_SLN_CASE(4, 1) EP_SLN_CASE(8, 1) EP_SLN_CASE(16, 1)
     EP_SLN_CASE(32, 1) EP_SLN_CASE(32, 2) EP_SLN_CASE(32, 4) EP_SLN_CASE(32, 8)
     EP_SLN_CASE(64, 8) EP_SLN_CASE(128, 8) EP_SLN_CASE(256, 8) EP_SLN_CASE(512, 8)
   } else {
@@ -491,34 +493,68 @@ KernelFn pick_kernel(int64_t H, int* tpr_out) {
   return nullptr;
 }
 
-// Row shapes of the staged kernel: the first threads-per-row TPR (in this
-// order) whose NV <= 8 fragments per thread hold the row and whose tile of
-// RT = 256/TPR rows is at most kTmaTileBytes (TPR = 256 takes any tile).
+// Row shapes of the staged kernel.  A row of nfrag = H/VW 16-byte fragments
+// is split over TPR threads (a power of two, 16 to 256) holding NV fragments
+// each; a CTA's 256 consumer threads take RT = 256/TPR rows per tile.
+//
+// Measured on GB300 (64 MB operands, every hidden size from 256 to 8192), a
+// shape that covers the row exactly runs at the copy bandwidth when NV is 3 to
+// 5; NV = 6 to 8 of 8-half fragments loses up to a fifth, and a ragged shape
+// (idle lanes in the last fragment column) a quarter.  So the exact shape with
+// the smallest NV >= 3 (TPR = nfrag/NV, the largest such power of two) is
+// taken, then NV = 2 (one 16-thread group per 32-fragment row).  Rows with no
+// exact shape take the first TPR whose NV <= 8 fragments hold the row and whose
+// tile is at most kTmaTileBytes (TPR = 256 takes any tile).
 constexpr uint32_t kTmaTileBytes = EP_SLN_TMA_TILE_BYTES;
 constexpr uint32_t kTmaStageBudget = EP_SLN_TMA_STAGE_BUDGET;  // shared memory for the stages of one CTA
 
 using TmaFn = void (*)(SlnKernelArgs, int, int64_t, uint32_t);
 
+// the power-of-two TPR in [16, 256] with TPR*nv == nfrag, else 0
+inline int exact_tpr(int64_t nfrag, int nv) {
+  if (nfrag % nv != 0) return 0;
+  const int64_t t = nfrag / nv;
+  return (t >= 16 && t <= 256 && (t & (t - 1)) == 0) ? static_cast<int>(t) : 0;
+}
+
 template <typename T>
 TmaFn pick_tma_kernel(int64_t H, int* rows_per_tile) {
   constexpr int VW = dev::Vec16<T>::N;
   const int64_t nfrag = H / VW;
-  const int64_t row_bytes = H * int64_t(sizeof(T));
   if (nfrag < 32) return nullptr;
-  const int tprs[] = {16, 32, 64, 128, 256};
-  for (int tpr : tprs) {
+  // exact shapes; the compiled set is every (TPR, NV) this search can return
+  for (int nv : {3, 4, 5, 6, 7, 8, 2}) {
+    const int tpr = exact_tpr(nfrag, nv);
+    if (tpr == 0) continue;
+    *rows_per_tile = kWsConsumers / tpr;
+#define EP_SLN_TMA_EXACT(TPR_, NV_) \
+    if (tpr == TPR_ && nv == NV_) return k_skip_layer_norm_tma<T, TPR_, NV_, true>;
+    EP_SLN_TMA_EXACT(16, 3) EP_SLN_TMA_EXACT(32, 3) EP_SLN_TMA_EXACT(64, 3) EP_SLN_TMA_EXACT(128, 3)
+    EP_SLN_TMA_EXACT(256, 3)
+    EP_SLN_TMA_EXACT(16, 4) EP_SLN_TMA_EXACT(32, 4) EP_SLN_TMA_EXACT(64, 4) EP_SLN_TMA_EXACT(128, 4)
+    EP_SLN_TMA_EXACT(256, 4)
+    EP_SLN_TMA_EXACT(16, 5) EP_SLN_TMA_EXACT(32, 5) EP_SLN_TMA_EXACT(64, 5) EP_SLN_TMA_EXACT(128, 5)
+    EP_SLN_TMA_EXACT(256, 5)
+    EP_SLN_TMA_EXACT(256, 6)  // NV = 6 or 8 below TPR = 256 is NV = 3 or 4 at twice the TPR
+    EP_SLN_TMA_EXACT(16, 7) EP_SLN_TMA_EXACT(32, 7) EP_SLN_TMA_EXACT(64, 7) EP_SLN_TMA_EXACT(128, 7)
+    EP_SLN_TMA_EXACT(256, 7)
+    EP_SLN_TMA_EXACT(256, 8)
+    EP_SLN_TMA_EXACT(16, 2)   // NV = 2 is reached only for nfrag = 32
+#undef EP_SLN_TMA_EXACT
+    return nullptr;
+  }
+  const int64_t row_bytes = H * int64_t(sizeof(T));
+  for (int tpr : {16, 32, 64, 128, 256}) {
     const int64_t nv = (nfrag + tpr - 1) / tpr;
     if (nv > 8) continue;
     const int rt = kWsConsumers / tpr;
     if (rt * row_bytes > kTmaTileBytes && tpr != 256) continue;
     *rows_per_tile = rt;
-#define EP_SLN_TMA_CASE(TPR_, NV_)                                                \
-  if (tpr == TPR_ && nv <= NV_)                                                  \
-    return nfrag == int64_t(TPR_) * NV_ ? k_skip_layer_norm_tma<T, TPR_, NV_, true> \
-                                        : k_skip_layer_norm_tma<T, TPR_, NV_, false>;
-    EP_SLN_TMA_CASE(16, 2) EP_SLN_TMA_CASE(16, 4) EP_SLN_TMA_CASE(32, 4) EP_SLN_TMA_CASE(64, 4) EP_SLN_TMA_CASE(128, 4)
-    EP_SLN_TMA_CASE(256, 4) EP_SLN_TMA_CASE(256, 8)
-#undef EP_SLN_TMA_CASE
+#define EP_SLN_TMA_RAGGED(TPR_, NV_) \
+    if (tpr == TPR_ && nv <= NV_) return k_skip_layer_norm_tma<T, TPR_, NV_, false>;
+    EP_SLN_TMA_RAGGED(16, 4) EP_SLN_TMA_RAGGED(32, 4) EP_SLN_TMA_RAGGED(64, 4) EP_SLN_TMA_RAGGED(128, 4)
+    EP_SLN_TMA_RAGGED(256, 4) EP_SLN_TMA_RAGGED(256, 8)
+#undef EP_SLN_TMA_RAGGED
     return nullptr;
   }
   return nullptr;
