@@ -247,6 +247,23 @@ def test_split_path_several_windows(lib, dtype, rows, cols, bias_rows, inner):
     np.testing.assert_allclose(to_np64(out).sum(axis=1), 1.0, atol=5e-3 if dtype == "f16" else 1e-4)
 
 
+# Split rows whose chunk ranges cross rows at odd places, and rows of 2.5 M
+# and 4 M elements (over a thousand chunks each, spread over every CTA).
+@pytest.mark.parametrize("dtype,rows,cols,bias_rows,inner", [
+    ("f32", 37, 300000, 37, 0), ("f16", 29, 600000, 1, 1), ("bf16", 23, 333336, 23, 1),
+    ("f32", 2, (1 << 22) + 8, 1, 0), ("f16", 2, (1 << 22) + 8, 2, 1), ("f32", 1, 2490368, 1, 0),
+])
+def test_split_odd_ranges_and_very_long_rows(lib, dtype, rows, cols, bias_rows, inner):
+    d = synth.bias_softmax_inputs((rows, cols), (bias_rows, cols), dtype, data_std=2.0, seed=rows + cols)
+    out = run(lib, d["data"], d["bias"], 1, inner)
+    sample = sorted(set(synth.sample_rows(rows, 6)) | {0, rows - 1})
+    check(d["data"], d["bias"], 1, inner, out, rows=sample)
+    # row sums: float16 outputs near 1/cols are subnormal (step 2^-24), so each
+    # may be off by 2^-25 in absolute terms
+    atol = 1e-4 if dtype == "f32" else 5e-3 + (cols * 2.0 ** -25 if dtype == "f16" else 0.0)
+    np.testing.assert_allclose(to_np64(out).sum(axis=1), 1.0, atol=atol)
+
+
 @pytest.mark.parametrize("dtype,cols", [("f32", 40000), ("f16", 70000), ("bf16", 70000)])
 def test_split_ranges_cross_rows_with_masked_chunks(lib, dtype, cols):
     # more chunks than one wave of CTAs, so a CTA's range of chunks runs from the
