@@ -320,6 +320,31 @@ def test_ex_simplified_and_statistics(lib, simplified, dtype, shape, skip_shape,
         assert (mean == 0).all()
 
 
+@pytest.mark.parametrize("dtype,rows,H", [
+    ("f32", 320000, 771),     # register kernel: two 128-thread rows per CTA, about two rounds of the grid
+    ("f16", 6000, 16400),     # three-pass kernel, more rows than CTAs
+])
+def test_ex_simplified_many_rows_per_cta(lib, dtype, rows, H):
+    # the RMS form has one reduction per row; consecutive rows of a CTA must
+    # not share its shared-memory buffer.  Inputs are drawn on the device.
+    x = synth.device_normal((rows, H), dtype, seed=rows)
+    sk = synth.device_normal((rows, H), dtype, seed=rows + 1)
+    g = (synth.device_normal((H,), dtype, seed=rows + 2, std=0.1).float() + 1.0).to(x.dtype)
+    bt = synth.device_normal((H,), dtype, seed=rows + 3, std=0.1)
+    out = torch.empty_like(x)
+    inv = torch.empty(rows, dtype=torch.float32, device="cuda")
+    lib.ep_skip_layer_norm_ex(x, sk, g, bt, None, 1e-5, simplified=True, output=out, inv_std_dev=inv)
+    torch.cuda.synchronize()
+    sample = torch.tensor(sorted(set(synth.sample_rows(rows, 300)) | set(range(rows - 5, rows))))
+    o = oracle.skip_layer_norm(x[sample.cuda()].cpu(), sk[sample.cuda()].cpu(), g.cpu(), bt.cpu(), None, 1e-5,
+                               simplified=True)
+    assert_norm_close(out[sample.cuda()].cpu(), o["output"], x.dtype)
+    np.testing.assert_allclose(inv[sample.cuda()].cpu().numpy().astype(np.float64), o["inv_std_dev"],
+                               rtol=2e-5, atol=0)
+    del x, sk, out
+    torch.cuda.empty_cache()
+
+
 def test_ex_default_matches_plain_entry_point(lib):
     d = synth.sln_inputs((33, 1024), None, "f16", has_beta=True, has_bias=True, seed=4)
     a, s_a = run(lib, d, residual=True)

@@ -57,8 +57,14 @@ k_skip_layer_norm(const SlnKernelArgs a) {
   dev::pdl_trigger();
   constexpr int BS = TPR > 256 ? TPR : 256;
   constexpr int RPC = BS / TPR;  // rows per CTA
+  // red_a: the mean; red_b: the variance, by row parity.  A row's reads of a
+  // buffer precede the next write to it only through a barrier between them:
+  // red_a is next written after this row's variance barrier, and the variance
+  // buffer two rows on, after the next row's variance barrier (the RMS form has
+  // no mean barrier).
   __shared__ float red_a[BS / 32];
-  __shared__ float red_b[BS / 32];
+  __shared__ float red_b[2][BS / 32];
+  int par = 0;
 
   // input/skip may be the same buffers as output/sum_out (exact in-place
   // aliasing), so only the never-written vectors are marked __restrict__.
@@ -136,7 +142,8 @@ k_skip_layer_norm(const SlnKernelArgs a) {
         }
       }
     }
-    const float var = dev::group_sum<TPR>(q, red_b) / static_cast<float>(H);
+    const float var = dev::group_sum<TPR>(q, red_b[par]) / static_cast<float>(H);
+    par ^= 1;
     const float rstd = 1.0f / sqrtf(var + a.eps);
 
     if (active) {
@@ -172,7 +179,8 @@ __global__ void __launch_bounds__(1024) k_skip_layer_norm_long(const SlnKernelAr
   dev::pdl_wait();
   dev::pdl_trigger();
   __shared__ float red_a[32];
-  __shared__ float red_b[32];
+  __shared__ float red_b[2][32];  // by row parity, as in k_skip_layer_norm
+  int par = 0;
   const T* in = static_cast<const T*>(a.input);
   const T* sk = static_cast<const T*>(a.skip);
   const T* gamma = static_cast<const T*>(a.gamma);
@@ -203,7 +211,8 @@ __global__ void __launch_bounds__(1024) k_skip_layer_norm_long(const SlnKernelAr
       const float d = s_at(off, soff, c) - mean;
       q = fmaf(d, d, q);
     }
-    const float var = dev::group_sum<1024>(q, red_b) / static_cast<float>(H);
+    const float var = dev::group_sum<1024>(q, red_b[par]) / static_cast<float>(H);
+    par ^= 1;
     const float rstd = 1.0f / sqrtf(var + a.eps);
     if (threadIdx.x == 0) {
       if (a.mean_out != nullptr) a.mean_out[r] = mean;
@@ -216,8 +225,6 @@ __global__ void __launch_bounds__(1024) k_skip_layer_norm_long(const SlnKernelAr
       const float gm = dev::ld1_keep(gamma + c);
       dev::st1_stream(out + off + c, beta != nullptr ? fmaf(n, gm, dev::ld1_keep(beta + c)) : n * gm);
     }
-    // red_a/red_b are reused by the next row: the next write to red_a follows
-    // this row's second barrier, which every thread passes only after reading red_a.
   }
 }
 
