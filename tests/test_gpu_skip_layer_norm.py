@@ -90,8 +90,10 @@ def test_hidden_sizes(lib, dtype, H):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
-@pytest.mark.parametrize("H", [16385, 20000, 40000])
-def test_long_rows_three_pass(lib, dtype, H):
+@pytest.mark.parametrize("H", [16385, 16392, 20000, 24576, 32768, 32776, 40000])
+def test_long_rows(lib, dtype, H):
+    # aligned rows up to 32768: 1024-thread register shapes; others and longer
+    # rows: the three-pass kernel
     d = synth.sln_inputs((3, H), None, dtype, has_beta=True, has_bias=True, seed=H)
     out, s = run(lib, d, residual=True)
     check(d, out, s)
@@ -322,7 +324,8 @@ def test_ex_simplified_and_statistics(lib, simplified, dtype, shape, skip_shape,
 
 @pytest.mark.parametrize("dtype,rows,H", [
     ("f32", 320000, 771),     # register kernel: two 128-thread rows per CTA, about two rounds of the grid
-    ("f16", 6000, 16400),     # three-pass kernel, more rows than CTAs
+    ("f16", 20000, 20000),    # 1024-thread register rows, more rows than CTAs
+    ("f16", 6000, 16401),     # three-pass kernel, more rows than CTAs
 ])
 def test_ex_simplified_many_rows_per_cta(lib, dtype, rows, H):
     # the RMS form has one reduction per row; consecutive rows of a CTA must
