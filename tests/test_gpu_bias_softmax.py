@@ -190,7 +190,7 @@ def test_workload_long_rows_full(lib, name, inner):
 # (the last fragment column partly idle), several tiles of 256/TPR rows with a
 # partial last tile, bias broadcast both ways; and the sub-warp register shapes
 # (rows of 1 to 16 fragments held by 4 to 16 threads) over several CTAs.
-_EXACT_SHAPES = [(t, nv) for nv in (4, 5, 6, 7) for t in (16, 32, 64, 128, 256)] + [(256, 8), (16, 3), (16, 2)]
+_EXACT_SHAPES = [(t, nv) for nv in (4, 5, 6, 7) for t in (4, 8, 16, 32, 64, 128, 256)] + [(256, 8), (4, 3)]
 _RAGGED_NFRAG = [40, 100, 200, 300, 700, 1500]   # 16x4, 32x4, 64x4, 128x4, 256x4, 256x8 with idle lanes
 
 
@@ -204,7 +204,7 @@ def _shape_cases():
 
 @pytest.mark.parametrize("dtype,cols", _shape_cases())
 def test_staged_row_shapes(lib, dtype, cols):
-    rows, bias_rows = (115, 5) if cols <= 4096 else (40, 5)   # >= 7 tiles of up to 16 rows; >= 20 of 1 or 2
+    rows, bias_rows = (455, 5) if cols <= 1024 else (115, 5) if cols <= 4096 else (40, 5)  # >= 7 tiles of 64, 16 or 2 rows
     d = synth.bias_softmax_inputs((rows, cols), (bias_rows, cols), dtype, data_std=3.0, seed=cols)
     for inner in (0, 1):
         out = run(lib, d["data"], d["bias"], 1, inner)
@@ -226,6 +226,7 @@ def test_subwarp_register_shapes(lib, dtype, nfrag):
     ("f16", 80003, 512, 11429, 1), ("f16", 80003, 512, 11429, 0), ("f16", 80003, 512, 7, 0),
     ("f16", 80003, 512, 7, 1), ("f32", 40000, 256, 40000, 0), ("f32", 30000, 1024, 3, 1),
     ("f16", 10000, 4096, 10, 0), ("f32", 9001, 2048, 9001, 1),
+    ("f16", 40000, 128, 8, 0), ("f16", 40000, 96, 2500, 1), ("f32", 30000, 64, 30000, 0),   # 64-row tiles
 ])
 def test_staged_many_tiles(lib, dtype, rows, cols, bias_rows, inner):
     d = synth.bias_softmax_inputs((rows, cols), (bias_rows, cols), dtype, data_std=3.0, seed=rows + bias_rows)

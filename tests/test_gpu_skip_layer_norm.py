@@ -227,6 +227,7 @@ def test_workload_full_size_sampled_rows(lib, name):
 @pytest.mark.parametrize("dtype,H,rows,skip_rows", [
     ("f32", 1024, 20001, None), ("f16", 4096, 6003, None), ("f32", 1024, 20000, 2000),
     ("f32", 768, 12007, 12007), ("f16", 2048, 9000, 3), ("f16", 512, 30001, 30001),
+    ("f16", 32, 21000, 7), ("f32", 64, 9001, 9001), ("bf16", 128, 40000, 5),   # 64-row tiles
 ])
 def test_staged_many_tiles(lib, dtype, H, rows, skip_rows):
     if skip_rows is None or skip_rows == rows:
@@ -244,10 +245,12 @@ def test_staged_many_tiles(lib, dtype, H, rows, skip_rows):
 # 16-byte fragments of a row.  Exact shapes (H = TPR*NV*VW) and ragged ones
 # (the last fragment column partly idle), each over several tiles of 256/TPR
 # rows with a partial last tile; and the sub-warp register shapes (a row of
-# 1 to 16 fragments held by 4 to 16 threads) over several CTAs.
+# 1 to 16 fragments held by 4 to 16 threads, for rows that are not 16-byte
+# aligned) over several CTAs.
 # ---------------------------------------------------------------------------
 
-_EXACT_SHAPES = [(t, nv) for nv in (3, 4, 5, 7) for t in (16, 32, 64, 128, 256)] + [(256, 6), (256, 8), (16, 2)]
+_EXACT_SHAPES = ([(t, nv) for nv in (3, 4, 5, 7) for t in (4, 8, 16, 32, 64, 128, 256)]
+                 + [(256, 6), (256, 8), (4, 2), (4, 1)])
 _RAGGED_NFRAG = [40, 100, 200, 300, 700, 1500]   # 16x4, 32x4, 64x4, 128x4, 256x4, 256x8 with idle lanes
 
 
@@ -261,7 +264,7 @@ def _shape_cases():
 
 @pytest.mark.parametrize("dtype,H", _shape_cases())
 def test_staged_row_shapes(lib, dtype, H):
-    rows = 115 if H <= 4096 else 37                # >= 7 tiles of up to 16 rows; >= 19 tiles of 1 or 2 rows
+    rows = 451 if H <= 1024 else 115 if H <= 4096 else 37   # >= 7 tiles of up to 64, 16 or 2 rows
     d = synth.sln_inputs((rows, H), None, dtype, has_beta=True, has_bias=True, seed=H + rows)
     out, s = run(lib, d, residual=True)
     check(d, out, s)

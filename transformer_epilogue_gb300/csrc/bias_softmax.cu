@@ -212,7 +212,7 @@ constexpr int kWsConsumers = 256;
 constexpr int kWsThreads = kWsConsumers + 32;
 constexpr int kWsConsumerWarps = kWsConsumers / 32;
 constexpr int kTmaMaxStages = 8;
-constexpr int kMaxTileRows = kWsConsumers / 16;
+constexpr int kMaxTileRows = kWsConsumers / 4;
 
 // EXACT: the row is exactly TPR*NV fragments, so no column needs a bounds check.
 template <typename T, int TPR, int NV, bool EXACT>
@@ -935,18 +935,22 @@ constexpr uint32_t kTmaTileBytes = EP_SM_TMA_TILE_BYTES;
 constexpr uint32_t kTmaStageBudget = EP_SM_TMA_STAGE_BUDGET;
 
 // Row shapes: a row of nfrag = cols/VW 16-byte fragments is split over TPR
-// threads (a power of two, 16 to 256) holding NV fragments each; a tile is
-// RT = 256/TPR rows.  Measured on GB300 (128 MB of data, row lengths 256 to
+// threads (a power of two, 4 to 256) holding NV fragments each; a tile is
+// RT = 256/TPR rows.  Measured on GB300 (128-256 MB of data, row lengths 32 to
 // 16384, bias broadcast either way), a shape that covers the row exactly beats
 // a ragged one by 10 to 30 %, and among exact shapes NV = 4 to 6 is best
 // (NV = 3 loses up to 5 %: the stage also carries bias rows, so fewer, fuller
 // threads per row pay off).  So the exact shape with the smallest NV >= 4,
-// then NV = 3, then NV = 2; rows with no exact shape take the first TPR whose
-// NV <= 8 fragments hold the row and whose data tile is at most kTmaTileBytes.
+// then NV = 3, then NV = 2.  Short rows take 4 or 8 threads a row: 96-192
+// columns of float16 went from 0.43-0.56 of the copy bandwidth on the register
+// kernel to 0.8-0.93; rows under 12 fragments stay on the register kernel (a
+// 4-thread row of 1 or 2 fragments measured slower).  Rows with no exact shape
+// and at least 32 fragments take the first TPR whose NV <= 8 fragments hold
+// the row and whose data tile is at most kTmaTileBytes.
 inline int exact_tpr(int64_t nfrag, int nv) {
   if (nfrag % nv != 0) return 0;
   const int64_t t = nfrag / nv;
-  return (t >= 16 && t <= 256 && (t & (t - 1)) == 0) ? static_cast<int>(t) : 0;
+  return (t >= 4 && t <= 256 && (t & (t - 1)) == 0) ? static_cast<int>(t) : 0;
 }
 
 template <typename T>
@@ -954,28 +958,29 @@ TmaRowFn pick_tma_row_kernel(int64_t cols, int* rows_per_tile) {
   constexpr int VW = dev::Vec16<T>::N;
   const int64_t nfrag = cols / VW;
   const int64_t row_bytes = cols * int64_t(sizeof(T));
-  if (nfrag < 32) return nullptr;
+  if (nfrag < 12) return nullptr;
   // exact shapes; the compiled set is every (TPR, NV) this search can return
-  for (int nv : {4, 5, 6, 7, 8, 3, 2}) {
+  for (int nv : {4, 5, 6, 7, 8, 3}) {
     const int tpr = exact_tpr(nfrag, nv);
     if (tpr == 0 || tpr < EP_SM_TMA_MIN_TPR) continue;
     *rows_per_tile = kWsConsumers / tpr;
 #define EP_SM_TMA_EXACT(TPR_, NV_) \
     if (tpr == TPR_ && nv == NV_) return k_bias_softmax_rows_tma<T, TPR_, NV_, true>;
-    EP_SM_TMA_EXACT(16, 4) EP_SM_TMA_EXACT(32, 4) EP_SM_TMA_EXACT(64, 4) EP_SM_TMA_EXACT(128, 4)
-    EP_SM_TMA_EXACT(256, 4)
-    EP_SM_TMA_EXACT(16, 5) EP_SM_TMA_EXACT(32, 5) EP_SM_TMA_EXACT(64, 5) EP_SM_TMA_EXACT(128, 5)
-    EP_SM_TMA_EXACT(256, 5)
-    EP_SM_TMA_EXACT(16, 6) EP_SM_TMA_EXACT(32, 6) EP_SM_TMA_EXACT(64, 6) EP_SM_TMA_EXACT(128, 6)
-    EP_SM_TMA_EXACT(256, 6)
-    EP_SM_TMA_EXACT(16, 7) EP_SM_TMA_EXACT(32, 7) EP_SM_TMA_EXACT(64, 7) EP_SM_TMA_EXACT(128, 7)
-    EP_SM_TMA_EXACT(256, 7)
+    EP_SM_TMA_EXACT(4, 4) EP_SM_TMA_EXACT(8, 4) EP_SM_TMA_EXACT(16, 4) EP_SM_TMA_EXACT(32, 4)
+    EP_SM_TMA_EXACT(64, 4) EP_SM_TMA_EXACT(128, 4) EP_SM_TMA_EXACT(256, 4)
+    EP_SM_TMA_EXACT(4, 5) EP_SM_TMA_EXACT(8, 5) EP_SM_TMA_EXACT(16, 5) EP_SM_TMA_EXACT(32, 5)
+    EP_SM_TMA_EXACT(64, 5) EP_SM_TMA_EXACT(128, 5) EP_SM_TMA_EXACT(256, 5)
+    EP_SM_TMA_EXACT(4, 6) EP_SM_TMA_EXACT(8, 6) EP_SM_TMA_EXACT(16, 6) EP_SM_TMA_EXACT(32, 6)
+    EP_SM_TMA_EXACT(64, 6) EP_SM_TMA_EXACT(128, 6) EP_SM_TMA_EXACT(256, 6)
+    EP_SM_TMA_EXACT(4, 7) EP_SM_TMA_EXACT(8, 7) EP_SM_TMA_EXACT(16, 7) EP_SM_TMA_EXACT(32, 7)
+    EP_SM_TMA_EXACT(64, 7) EP_SM_TMA_EXACT(128, 7) EP_SM_TMA_EXACT(256, 7)
     EP_SM_TMA_EXACT(256, 8)   // NV = 8 below TPR = 256 is NV = 4 at twice the TPR
-    EP_SM_TMA_EXACT(16, 3)    // NV = 3 above TPR = 16 is NV = 6 at half the TPR
-    EP_SM_TMA_EXACT(16, 2)    // NV = 2 is reached only for nfrag = 32
+    EP_SM_TMA_EXACT(4, 3)     // NV = 3 above TPR = 4 is NV = 6 at half the TPR; NV = 2 is never
+                              // reached (nfrag = 2 TPR is NV = 4 at TPR / 2, or under 12 fragments)
 #undef EP_SM_TMA_EXACT
     return nullptr;
   }
+  if (nfrag < 32) return nullptr;
   for (int tpr : {16, 32, 64, 128, 256}) {
     const int64_t nv = (nfrag + tpr - 1) / tpr;
     if (nv > 8 || tpr < EP_SM_TMA_MIN_TPR) continue;

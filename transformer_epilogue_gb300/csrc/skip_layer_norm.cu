@@ -503,55 +503,60 @@ KernelFn pick_kernel(int64_t H, int* tpr_out) {
 }
 
 // Row shapes of the staged kernel.  A row of nfrag = H/VW 16-byte fragments
-// is split over TPR threads (a power of two, 16 to 256) holding NV fragments
+// is split over TPR threads (a power of two, 4 to 256) holding NV fragments
 // each; a CTA's 256 consumer threads take RT = 256/TPR rows per tile.
 //
-// Measured on GB300 (64 MB operands, every hidden size from 256 to 8192), a
-// shape that covers the row exactly runs at the copy bandwidth when NV is 3 to
-// 5; NV = 6 to 8 of 8-half fragments loses up to a fifth, and a ragged shape
-// (idle lanes in the last fragment column) a quarter.  So the exact shape with
-// the smallest NV >= 3 (TPR = nfrag/NV, the largest such power of two) is
-// taken, then NV = 2 (one 16-thread group per 32-fragment row).  Rows with no
-// exact shape take the first TPR whose NV <= 8 fragments hold the row and whose
-// tile is at most kTmaTileBytes (TPR = 256 takes any tile).
+// Measured on GB300 (64-256 MB operands, hidden sizes 32 to 8192), a shape
+// that covers the row exactly runs at the copy bandwidth when NV is 3 to 5;
+// NV = 6 to 8 of 8-half fragments loses up to a fifth, and a ragged shape (idle
+// lanes in the last fragment column) a quarter.  So the exact shape with the
+// smallest NV >= 3 (TPR = nfrag/NV, the largest such power of two) is taken,
+// then NV = 2 and 1 (rows of 8 and 4 fragments).  Short rows take 4 or 8
+// threads a row (64 or 32 rows a tile): H = 32-128 in float16 went from 0.55-0.72
+// of the copy bandwidth on the register kernel to 0.8-1.04.  Rows with no
+// exact shape and at least 32 fragments take the first TPR whose NV <= 8
+// fragments hold the row and whose tile is at most kTmaTileBytes (TPR = 256
+// takes any tile); shorter ones the register kernel.
 constexpr uint32_t kTmaTileBytes = EP_SLN_TMA_TILE_BYTES;
 constexpr uint32_t kTmaStageBudget = EP_SLN_TMA_STAGE_BUDGET;  // shared memory for the stages of one CTA
 
 using TmaFn = void (*)(SlnKernelArgs, int, int64_t, uint32_t);
 
-// the power-of-two TPR in [16, 256] with TPR*nv == nfrag, else 0
+// the power-of-two TPR in [4, 256] with TPR*nv == nfrag, else 0
 inline int exact_tpr(int64_t nfrag, int nv) {
   if (nfrag % nv != 0) return 0;
   const int64_t t = nfrag / nv;
-  return (t >= 16 && t <= 256 && (t & (t - 1)) == 0) ? static_cast<int>(t) : 0;
+  return (t >= 4 && t <= 256 && (t & (t - 1)) == 0) ? static_cast<int>(t) : 0;
 }
 
 template <typename T>
 TmaFn pick_tma_kernel(int64_t H, int* rows_per_tile) {
   constexpr int VW = dev::Vec16<T>::N;
   const int64_t nfrag = H / VW;
-  if (nfrag < 32) return nullptr;
+  if (nfrag < 4) return nullptr;
   // exact shapes; the compiled set is every (TPR, NV) this search can return
-  for (int nv : {3, 4, 5, 6, 7, 8, 2}) {
+  for (int nv : {3, 4, 5, 6, 7, 8, 2, 1}) {
     const int tpr = exact_tpr(nfrag, nv);
     if (tpr == 0) continue;
     *rows_per_tile = kWsConsumers / tpr;
 #define EP_SLN_TMA_EXACT(TPR_, NV_) \
     if (tpr == TPR_ && nv == NV_) return k_skip_layer_norm_tma<T, TPR_, NV_, true>;
-    EP_SLN_TMA_EXACT(16, 3) EP_SLN_TMA_EXACT(32, 3) EP_SLN_TMA_EXACT(64, 3) EP_SLN_TMA_EXACT(128, 3)
-    EP_SLN_TMA_EXACT(256, 3)
-    EP_SLN_TMA_EXACT(16, 4) EP_SLN_TMA_EXACT(32, 4) EP_SLN_TMA_EXACT(64, 4) EP_SLN_TMA_EXACT(128, 4)
-    EP_SLN_TMA_EXACT(256, 4)
-    EP_SLN_TMA_EXACT(16, 5) EP_SLN_TMA_EXACT(32, 5) EP_SLN_TMA_EXACT(64, 5) EP_SLN_TMA_EXACT(128, 5)
-    EP_SLN_TMA_EXACT(256, 5)
+    EP_SLN_TMA_EXACT(4, 3) EP_SLN_TMA_EXACT(8, 3) EP_SLN_TMA_EXACT(16, 3) EP_SLN_TMA_EXACT(32, 3)
+    EP_SLN_TMA_EXACT(64, 3) EP_SLN_TMA_EXACT(128, 3) EP_SLN_TMA_EXACT(256, 3)
+    EP_SLN_TMA_EXACT(4, 4) EP_SLN_TMA_EXACT(8, 4) EP_SLN_TMA_EXACT(16, 4) EP_SLN_TMA_EXACT(32, 4)
+    EP_SLN_TMA_EXACT(64, 4) EP_SLN_TMA_EXACT(128, 4) EP_SLN_TMA_EXACT(256, 4)
+    EP_SLN_TMA_EXACT(4, 5) EP_SLN_TMA_EXACT(8, 5) EP_SLN_TMA_EXACT(16, 5) EP_SLN_TMA_EXACT(32, 5)
+    EP_SLN_TMA_EXACT(64, 5) EP_SLN_TMA_EXACT(128, 5) EP_SLN_TMA_EXACT(256, 5)
     EP_SLN_TMA_EXACT(256, 6)  // NV = 6 or 8 below TPR = 256 is NV = 3 or 4 at twice the TPR
-    EP_SLN_TMA_EXACT(16, 7) EP_SLN_TMA_EXACT(32, 7) EP_SLN_TMA_EXACT(64, 7) EP_SLN_TMA_EXACT(128, 7)
-    EP_SLN_TMA_EXACT(256, 7)
+    EP_SLN_TMA_EXACT(4, 7) EP_SLN_TMA_EXACT(8, 7) EP_SLN_TMA_EXACT(16, 7) EP_SLN_TMA_EXACT(32, 7)
+    EP_SLN_TMA_EXACT(64, 7) EP_SLN_TMA_EXACT(128, 7) EP_SLN_TMA_EXACT(256, 7)
     EP_SLN_TMA_EXACT(256, 8)
-    EP_SLN_TMA_EXACT(16, 2)   // NV = 2 is reached only for nfrag = 32
+    EP_SLN_TMA_EXACT(4, 2)    // NV = 2 and 1 are reached only for nfrag = 8 and 4
+    EP_SLN_TMA_EXACT(4, 1)
 #undef EP_SLN_TMA_EXACT
     return nullptr;
   }
+  if (nfrag < 32) return nullptr;
   const int64_t row_bytes = H * int64_t(sizeof(T));
   for (int tpr : {16, 32, 64, 128, 256}) {
     const int64_t nv = (nfrag + tpr - 1) / tpr;

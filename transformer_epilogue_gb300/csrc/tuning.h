@@ -55,7 +55,7 @@
 #define EP_SM_CLC 1
 #endif
 #ifndef EP_SM_TMA_MIN_TPR
-#define EP_SM_TMA_MIN_TPR 16
+#define EP_SM_TMA_MIN_TPR 4
 #endif
 
 // Split-row softmax (rows longer than the row kernels hold): bytes of data in
