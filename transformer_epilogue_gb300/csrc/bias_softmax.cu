@@ -212,7 +212,6 @@ constexpr int kWsConsumers = 256;
 constexpr int kWsThreads = kWsConsumers + 32;
 constexpr int kWsConsumerWarps = kWsConsumers / 32;
 constexpr int kTmaMaxStages = 8;
-constexpr int kMaxTileRows = kWsConsumers / 4;
 
 // EXACT: the row is exactly TPR*NV fragments, so no column needs a bounds check.
 template <typename T, int TPR, int NV, bool EXACT>
@@ -226,7 +225,7 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
   __shared__ __align__(8) uint64_t clc_bar;
   __shared__ __align__(16) uint4 clc_resp;
   __shared__ int64_t tile_of[kTmaMaxStages];  // stage header: the tile, or -1
-  __shared__ int slot_of[kTmaMaxStages][kMaxTileRows];
+  __shared__ int slot_of[kTmaMaxStages][RT];  // sized per shape: static shared memory counts toward occupancy
   __shared__ float red_a[kWsConsumerWarps];
   __shared__ float red_b[kWsConsumerWarps];
 
