@@ -428,7 +428,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=ORDER, help="run only this workload --reps times (for ncu)")
     ap.add_argument("--batch", type=int, default=0, help="with --profile: cut the leading dimension to this")
@@ -514,9 +514,28 @@ def main(argv=None):
     total_ms = t_start.elapsed_time(t_end)
     dom_ms = statistics.fmean(a.elapsed_time(b) for a, b in dom_ev.values())
 
-    # e2e: pinned host inputs -> device, op, outputs -> pinned host, per step
-    pinned_in = [{k: hosts[n][k].pin_memory() for k in w.inputs} for n, w in zip(ORDER, work)]
-    pinned_out = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in w.outs.items()} for w in work]
+    # e2e: pinned host inputs -> device, op, outputs -> pinned host, per step.
+    # All pinned buffers are views of one page-locked block per direction (two
+    # host allocations, not one per tensor).
+    def pinned_views(tensors):
+        sizes = [(nbytes(t) + 255) // 256 * 256 for t in tensors]
+        block = torch.empty(sum(sizes), dtype=torch.uint8, pin_memory=True)
+        views, off = [], 0
+        for t, sz in zip(tensors, sizes):
+            views.append(block[off:off + nbytes(t)].view(t.dtype).view(t.shape))
+            off += sz
+        return views
+    in_src = [(i, k, hosts[n][k]) for i, (n, w) in enumerate(zip(ORDER, work)) for k in w.inputs]
+    in_views = pinned_views([t for _, _, t in in_src])
+    pinned_in = [{} for _ in work]
+    for (i, k, t), v in zip(in_src, in_views):
+        v.copy_(t)
+        pinned_in[i][k] = v
+    out_src = [(i, k, v) for i, w in enumerate(work) for k, v in w.outs.items()]
+    out_views = pinned_views([v for _, _, v in out_src])
+    pinned_out = [{} for _ in work]
+    for (i, k, _), v in zip(out_src, out_views):
+        pinned_out[i][k] = v
     h2d = sum(nbytes(t) for p in pinned_in for t in p.values())
     d2h = sum(nbytes(t) for p in pinned_out for t in p.values())
 
