@@ -214,11 +214,16 @@ constexpr int kWsConsumerWarps = kWsConsumers / 32;
 constexpr int kTmaMaxStages = 8;
 
 // EXACT: the row is exactly TPR*NV fragments, so no column needs a bounds check.
-template <typename T, int TPR, int NV, bool EXACT>
+// HALVES (one 256-thread row a tile, exact, NV even): a tile takes two stages,
+// each with half of the data row and the same half of its bias row, so that a
+// stage is half as large and two CTAs fit on an SM; consumers load the first
+// half of their fragments from the first stage and the rest from the second.
+template <typename T, int TPR, int NV, bool EXACT, bool HALVES = false>
 __global__ void __launch_bounds__(kWsThreads, EP_SM_TMA_MIN_CTAS)
 k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_t ntiles) {
   constexpr int VW = dev::Vec16<T>::N;
   constexpr int RT = kWsConsumers / TPR;
+  static_assert(!HALVES || (RT == 1 && EXACT && NV % 2 == 0), "half stages: one exact row a tile, NV even");
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[kTmaMaxStages];
   __shared__ __align__(8) uint64_t empty[kTmaMaxStages];
@@ -230,7 +235,8 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
   __shared__ float red_b[kWsConsumerWarps];
 
   const int C = static_cast<int>(a.cols);  // staged rows are at most 64 KB
-  const uint32_t row_bytes = static_cast<uint32_t>(C) * uint32_t(sizeof(T));
+  // a stage holds a row, or with HALVES half a row (and the same half of bias)
+  const uint32_t row_bytes = static_cast<uint32_t>(C) * uint32_t(sizeof(T)) / (HALVES ? 2u : 1u);
   const uint32_t data_bytes = RT * row_bytes;
   const uint32_t stage_bytes = data_bytes + uint32_t(bias_slots) * row_bytes;
   const int tid = threadIdx.x;
@@ -301,11 +307,33 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
       }
       unsigned char* dst = smem + size_t(st) * stage_bytes;
       unsigned char* bdst = dst + data_bytes;
-      // the arrive releases the slot_of writes above to the consumers
-      dev::mbar_arrive_expect_tx(&full[st], uint32_t(nr) * row_bytes + uint32_t(n1 + n2) * row_bytes);
-      dev::bulk_g2s(dst, data + r0 * C, uint32_t(nr) * row_bytes, &full[st], pol_stream);
-      dev::bulk_g2s(bdst, bias + b0 * C, uint32_t(n1) * row_bytes, &full[st], pol_keep);
-      if (n2 > 0) dev::bulk_g2s(bdst + n1 * row_bytes, bias, uint32_t(n2) * row_bytes, &full[st], pol_keep);
+      if constexpr (HALVES) {
+        // first half here; the second half of the row in the next stage
+        dev::mbar_arrive_expect_tx(&full[st], 2u * row_bytes);
+        dev::bulk_g2s(dst, data + r0 * C, row_bytes, &full[st], pol_stream);
+        dev::bulk_g2s(bdst, bias + b0 * C, row_bytes, &full[st], pol_keep);
+        ++j;
+        ring.next();
+        const int st2 = ring.st;
+        if (j >= stages && !dev::mbar_wait(&empty[st2], ring.phase ^ 1u)) {
+          for (int64_t k = j - stages; k < j; ++k)
+            dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
+          clc.drain();
+          return;
+        }
+        tile_of[st2] = tile;
+        slot_of[st2][0] = 0;
+        unsigned char* dst2 = smem + size_t(st2) * stage_bytes;
+        dev::mbar_arrive_expect_tx(&full[st2], 2u * row_bytes);
+        dev::bulk_g2s(dst2, data + r0 * C + C / 2, row_bytes, &full[st2], pol_stream);
+        dev::bulk_g2s(dst2 + data_bytes, bias + b0 * C + C / 2, row_bytes, &full[st2], pol_keep);
+      } else {
+        // the arrive releases the slot_of writes above to the consumers
+        dev::mbar_arrive_expect_tx(&full[st], uint32_t(nr) * row_bytes + uint32_t(n1 + n2) * row_bytes);
+        dev::bulk_g2s(dst, data + r0 * C, uint32_t(nr) * row_bytes, &full[st], pol_stream);
+        dev::bulk_g2s(bdst, bias + b0 * C, uint32_t(n1) * row_bytes, &full[st], pol_keep);
+        if (n2 > 0) dev::bulk_g2s(bdst + n1 * row_bytes, bias, uint32_t(n2) * row_bytes, &full[st], pol_keep);
+      }
       if (use_clc) {
         tile = clc.next();
       } else {
@@ -336,27 +364,62 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
 
     const int64_t r = tile * RT + g;
     const bool active = r < a.rows;
-    const unsigned char* stage = smem + size_t(st) * stage_bytes;
-    const T* s_d = reinterpret_cast<const T*>(stage) + g * C;
-    const T* s_b = reinterpret_cast<const T*>(stage + data_bytes) + (active ? slot_of[st][g] : 0) * C;
-
     float z[NV][VW];
+    if constexpr (HALVES) {
+      // fragments v < NV/2 lie in the first half of the row (this stage),
+      // the others in the second (the next stage)
+      constexpr int HV = NV / 2;
+      const int CH = C / 2;
+      const T* s_d = reinterpret_cast<const T*>(smem + size_t(st) * stage_bytes);
+      const T* s_b = reinterpret_cast<const T*>(smem + size_t(st) * stage_bytes + data_bytes);
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      const int c = (v * TPR + lane) * VW;
-      if (active && (EXACT || c < C)) {
+      for (int v = 0; v < HV; ++v) {
+        const int c = (v * TPR + lane) * VW;
         float b[VW];
         dev::lds_unpack(s_d + c, z[v]);
         dev::lds_unpack(s_b + c, b);
 #pragma unroll
-        for (int e = 0; e < VW; ++e) z[v][e] += b[e];
-      } else {
-#pragma unroll
-        for (int e = 0; e < VW; ++e) z[v][e] = -INFINITY;
+        for (int e = 0; e < VW; ++e) z[v][e] = active ? z[v][e] + b[e] : -INFINITY;
       }
+      __syncwarp();
+      if ((tid & 31) == 0) dev::mbar_arrive(&empty[st]);
+      ring.next();
+      const int st2 = ring.st;
+      if (!dev::named_barrier_and(bar_id, TPR, dev::mbar_wait(&full[st2], ring.phase))) return;
+      const T* s_d2 = reinterpret_cast<const T*>(smem + size_t(st2) * stage_bytes);
+      const T* s_b2 = reinterpret_cast<const T*>(smem + size_t(st2) * stage_bytes + data_bytes);
+#pragma unroll
+      for (int v = HV; v < NV; ++v) {
+        const int c = (v * TPR + lane) * VW - CH;
+        float b[VW];
+        dev::lds_unpack(s_d2 + c, z[v]);
+        dev::lds_unpack(s_b2 + c, b);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) z[v][e] = active ? z[v][e] + b[e] : -INFINITY;
+      }
+      __syncwarp();
+      if ((tid & 31) == 0) dev::mbar_arrive(&empty[st2]);
+    } else {
+      const unsigned char* stage = smem + size_t(st) * stage_bytes;
+      const T* s_d = reinterpret_cast<const T*>(stage) + g * C;
+      const T* s_b = reinterpret_cast<const T*>(stage + data_bytes) + (active ? slot_of[st][g] : 0) * C;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int c = (v * TPR + lane) * VW;
+        if (active && (EXACT || c < C)) {
+          float b[VW];
+          dev::lds_unpack(s_d + c, z[v]);
+          dev::lds_unpack(s_b + c, b);
+#pragma unroll
+          for (int e = 0; e < VW; ++e) z[v][e] += b[e];
+        } else {
+#pragma unroll
+          for (int e = 0; e < VW; ++e) z[v][e] = -INFINITY;
+        }
+      }
+      __syncwarp();
+      if ((tid & 31) == 0) dev::mbar_arrive(&empty[st]);
     }
-    __syncwarp();
-    if ((tid & 31) == 0) dev::mbar_arrive(&empty[st]);
 
     float m = z[0][0];
 #pragma unroll
@@ -953,7 +1016,8 @@ inline int exact_tpr(int64_t nfrag, int nv) {
 }
 
 template <typename T>
-TmaRowFn pick_tma_row_kernel(int64_t cols, int* rows_per_tile) {
+TmaRowFn pick_tma_row_kernel(int64_t cols, int* rows_per_tile, bool* halves) {
+  *halves = false;
   constexpr int VW = dev::Vec16<T>::N;
   const int64_t nfrag = cols / VW;
   const int64_t row_bytes = cols * int64_t(sizeof(T));
@@ -973,7 +1037,12 @@ TmaRowFn pick_tma_row_kernel(int64_t cols, int* rows_per_tile) {
     EP_SM_TMA_EXACT(64, 6) EP_SM_TMA_EXACT(128, 6) EP_SM_TMA_EXACT(256, 6)
     EP_SM_TMA_EXACT(4, 7) EP_SM_TMA_EXACT(8, 7) EP_SM_TMA_EXACT(16, 7) EP_SM_TMA_EXACT(32, 7)
     EP_SM_TMA_EXACT(64, 7) EP_SM_TMA_EXACT(128, 7) EP_SM_TMA_EXACT(256, 7)
-    EP_SM_TMA_EXACT(256, 8)   // NV = 8 below TPR = 256 is NV = 4 at twice the TPR
+    // NV = 8 below TPR = 256 is NV = 4 at twice the TPR.  A 256x8 row is 32 KB:
+    // staged in halves, so that two CTAs (three stages each) fit on an SM
+    if (tpr == 256 && nv == 8) {
+      *halves = true;
+      return k_bias_softmax_rows_tma<T, 256, 8, true, true>;
+    }
     EP_SM_TMA_EXACT(4, 3)     // NV = 3 above TPR = 4 is NV = 6 at half the TPR; NV = 2 is never
                               // reached (nfrag = 2 TPR is NV = 4 at TPR / 2, or under 12 fragments)
 #undef EP_SM_TMA_EXACT
@@ -1000,14 +1069,17 @@ template <typename T>
 bool launch_tma_rows(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_count, cudaStream_t stream,
                      int* launches, cudaError_t* err) {
   int rt = 0;
-  TmaRowFn f = pick_tma_row_kernel<T>(a.cols, &rt);
+  bool halves = false;
+  TmaRowFn f = pick_tma_row_kernel<T>(a.cols, &rt, &halves);
   if (f == nullptr) return false;
-  const uint32_t row_bytes = uint32_t(a.cols * int64_t(sizeof(T)));
-  const int64_t slots = a.inner ? std::min<int64_t>(rt, (rt - 1) / a.inner_repeat + 2)
+  // a stage holds a tile (or with halves half a row) and its bias rows
+  const uint32_t row_bytes = uint32_t(a.cols * int64_t(sizeof(T))) / (halves ? 2u : 1u);
+  const int64_t slots = halves ? 1
+                      : a.inner ? std::min<int64_t>(rt, (rt - 1) / a.inner_repeat + 2)
                                 : std::min<int64_t>(rt, a.bias_rows);
   const uint32_t stage_bytes = uint32_t(rt + slots) * row_bytes;
   if (2 * stage_bytes > 2 * kTmaStageBudget) return false;
-  const int stages = std::min<int>(kTmaMaxStages, std::max<int>(2, kTmaStageBudget / stage_bytes));
+  const int stages = std::min<int>(kTmaMaxStages, std::max<int>(halves ? 3 : 2, kTmaStageBudget / stage_bytes));
   const size_t smem = size_t(stages) * stage_bytes;
   int per_sm = 1;
   *err = resident_ctas(reinterpret_cast<const void*>(f), kWsThreads, smem, &per_sm);
