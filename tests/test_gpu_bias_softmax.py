@@ -199,6 +199,7 @@ def _shape_cases():
     for dt, vw in (("f32", 4), ("f16", 8), ("bf16", 8)):
         out += [(dt, t * nv * vw) for t, nv in _EXACT_SHAPES]
         out += [(dt, nf * vw) for nf in _RAGGED_NFRAG]
+    out += [("f32", 256 * 12 * 4), ("f32", 256 * 16 * 4)]   # float32 rows staged in 3 and 4 parts
     return out
 
 

@@ -214,16 +214,17 @@ constexpr int kWsConsumerWarps = kWsConsumers / 32;
 constexpr int kTmaMaxStages = 8;
 
 // EXACT: the row is exactly TPR*NV fragments, so no column needs a bounds check.
-// HALVES (one 256-thread row a tile, exact, NV even): a tile takes two stages,
-// each with half of the data row and the same half of its bias row, so that a
-// stage is half as large and two CTAs fit on an SM; consumers load the first
-// half of their fragments from the first stage and the rest from the second.
-template <typename T, int TPR, int NV, bool EXACT, bool HALVES = false>
+// PARTS > 1 (one 256-thread row a tile, exact, NV a multiple of PARTS): a tile
+// takes PARTS consecutive stages, stage p holding part p of the data row
+// (columns [p C/PARTS, (p+1) C/PARTS)) and the same part of its bias row, so
+// that stages stay small and two CTAs fit on an SM.  A lane's fragments
+// v in [p NV/PARTS, (p+1) NV/PARTS) lie in part p.
+template <typename T, int TPR, int NV, bool EXACT, int PARTS = 1>
 __global__ void __launch_bounds__(kWsThreads, EP_SM_TMA_MIN_CTAS)
 k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_t ntiles) {
   constexpr int VW = dev::Vec16<T>::N;
   constexpr int RT = kWsConsumers / TPR;
-  static_assert(!HALVES || (RT == 1 && EXACT && NV % 2 == 0), "half stages: one exact row a tile, NV even");
+  static_assert(PARTS == 1 || (RT == 1 && EXACT && NV % PARTS == 0), "parts: one exact row a tile");
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[kTmaMaxStages];
   __shared__ __align__(8) uint64_t empty[kTmaMaxStages];
@@ -235,8 +236,8 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
   __shared__ float red_b[kWsConsumerWarps];
 
   const int C = static_cast<int>(a.cols);  // staged rows are at most 64 KB
-  // a stage holds a row, or with HALVES half a row (and the same half of bias)
-  const uint32_t row_bytes = static_cast<uint32_t>(C) * uint32_t(sizeof(T)) / (HALVES ? 2u : 1u);
+  // a stage holds rows, or one part of a row (and the same part of bias)
+  const uint32_t row_bytes = static_cast<uint32_t>(C) * uint32_t(sizeof(T)) / uint32_t(PARTS);
   const uint32_t data_bytes = RT * row_bytes;
   const uint32_t stage_bytes = data_bytes + uint32_t(bias_slots) * row_bytes;
   const int tid = threadIdx.x;
@@ -307,26 +308,29 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
       }
       unsigned char* dst = smem + size_t(st) * stage_bytes;
       unsigned char* bdst = dst + data_bytes;
-      if constexpr (HALVES) {
-        // first half here; the second half of the row in the next stage
+      if constexpr (PARTS > 1) {
+        // part 0 here, part p in the p-th stage after it
+        const int64_t part_cols = C / PARTS;
         dev::mbar_arrive_expect_tx(&full[st], 2u * row_bytes);
         dev::bulk_g2s(dst, data + r0 * C, row_bytes, &full[st], pol_stream);
         dev::bulk_g2s(bdst, bias + b0 * C, row_bytes, &full[st], pol_keep);
-        ++j;
-        ring.next();
-        const int st2 = ring.st;
-        if (j >= stages && !dev::mbar_wait(&empty[st2], ring.phase ^ 1u)) {
-          for (int64_t k = j - stages; k < j; ++k)
-            dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
-          clc.drain();
-          return;
+        for (int p = 1; p < PARTS; ++p) {
+          ++j;
+          ring.next();
+          const int sp = ring.st;
+          if (j >= stages && !dev::mbar_wait(&empty[sp], ring.phase ^ 1u)) {
+            for (int64_t k = j - stages; k < j; ++k)
+              dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
+            clc.drain();
+            return;
+          }
+          tile_of[sp] = tile;
+          slot_of[sp][0] = 0;
+          unsigned char* dp = smem + size_t(sp) * stage_bytes;
+          dev::mbar_arrive_expect_tx(&full[sp], 2u * row_bytes);
+          dev::bulk_g2s(dp, data + r0 * C + p * part_cols, row_bytes, &full[sp], pol_stream);
+          dev::bulk_g2s(dp + data_bytes, bias + b0 * C + p * part_cols, row_bytes, &full[sp], pol_keep);
         }
-        tile_of[st2] = tile;
-        slot_of[st2][0] = 0;
-        unsigned char* dst2 = smem + size_t(st2) * stage_bytes;
-        dev::mbar_arrive_expect_tx(&full[st2], 2u * row_bytes);
-        dev::bulk_g2s(dst2, data + r0 * C + C / 2, row_bytes, &full[st2], pol_stream);
-        dev::bulk_g2s(dst2 + data_bytes, bias + b0 * C + C / 2, row_bytes, &full[st2], pol_keep);
       } else {
         // the arrive releases the slot_of writes above to the consumers
         dev::mbar_arrive_expect_tx(&full[st], uint32_t(nr) * row_bytes + uint32_t(n1 + n2) * row_bytes);
@@ -365,40 +369,30 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
     const int64_t r = tile * RT + g;
     const bool active = r < a.rows;
     float z[NV][VW];
-    if constexpr (HALVES) {
-      // fragments v < NV/2 lie in the first half of the row (this stage),
-      // the others in the second (the next stage)
-      constexpr int HV = NV / 2;
-      const int CH = C / 2;
-      const T* s_d = reinterpret_cast<const T*>(smem + size_t(st) * stage_bytes);
-      const T* s_b = reinterpret_cast<const T*>(smem + size_t(st) * stage_bytes + data_bytes);
+    if constexpr (PARTS > 1) {
+      // part p of the row (fragments [p PV, (p+1) PV)) is in the p-th stage
+      constexpr int PV = NV / PARTS;
+      const int part_cols = C / PARTS;
 #pragma unroll
-      for (int v = 0; v < HV; ++v) {
-        const int c = (v * TPR + lane) * VW;
-        float b[VW];
-        dev::lds_unpack(s_d + c, z[v]);
-        dev::lds_unpack(s_b + c, b);
+      for (int p = 0; p < PARTS; ++p) {
+        if (p > 0) {
+          ring.next();
+          if (!dev::named_barrier_and(bar_id, TPR, dev::mbar_wait(&full[ring.st], ring.phase))) return;
+        }
+        const T* s_d = reinterpret_cast<const T*>(smem + size_t(ring.st) * stage_bytes);
+        const T* s_b = reinterpret_cast<const T*>(smem + size_t(ring.st) * stage_bytes + data_bytes);
 #pragma unroll
-        for (int e = 0; e < VW; ++e) z[v][e] = active ? z[v][e] + b[e] : -INFINITY;
+        for (int v = p * PV; v < (p + 1) * PV; ++v) {
+          const int c = (v * TPR + lane) * VW - p * part_cols;
+          float b[VW];
+          dev::lds_unpack(s_d + c, z[v]);
+          dev::lds_unpack(s_b + c, b);
+#pragma unroll
+          for (int e = 0; e < VW; ++e) z[v][e] = active ? z[v][e] + b[e] : -INFINITY;
+        }
+        __syncwarp();
+        if ((tid & 31) == 0) dev::mbar_arrive(&empty[ring.st]);
       }
-      __syncwarp();
-      if ((tid & 31) == 0) dev::mbar_arrive(&empty[st]);
-      ring.next();
-      const int st2 = ring.st;
-      if (!dev::named_barrier_and(bar_id, TPR, dev::mbar_wait(&full[st2], ring.phase))) return;
-      const T* s_d2 = reinterpret_cast<const T*>(smem + size_t(st2) * stage_bytes);
-      const T* s_b2 = reinterpret_cast<const T*>(smem + size_t(st2) * stage_bytes + data_bytes);
-#pragma unroll
-      for (int v = HV; v < NV; ++v) {
-        const int c = (v * TPR + lane) * VW - CH;
-        float b[VW];
-        dev::lds_unpack(s_d2 + c, z[v]);
-        dev::lds_unpack(s_b2 + c, b);
-#pragma unroll
-        for (int e = 0; e < VW; ++e) z[v][e] = active ? z[v][e] + b[e] : -INFINITY;
-      }
-      __syncwarp();
-      if ((tid & 31) == 0) dev::mbar_arrive(&empty[st2]);
     } else {
       const unsigned char* stage = smem + size_t(st) * stage_bytes;
       const T* s_d = reinterpret_cast<const T*>(stage) + g * C;
@@ -1016,14 +1010,14 @@ inline int exact_tpr(int64_t nfrag, int nv) {
 }
 
 template <typename T>
-TmaRowFn pick_tma_row_kernel(int64_t cols, int* rows_per_tile, bool* halves) {
-  *halves = false;
+TmaRowFn pick_tma_row_kernel(int64_t cols, int* rows_per_tile, int* parts) {
+  *parts = 1;
   constexpr int VW = dev::Vec16<T>::N;
   const int64_t nfrag = cols / VW;
   const int64_t row_bytes = cols * int64_t(sizeof(T));
   if (nfrag < 12) return nullptr;
   // exact shapes; the compiled set is every (TPR, NV) this search can return
-  for (int nv : {4, 5, 6, 7, 8, 3}) {
+  for (int nv : {4, 5, 6, 7, 8, 3, 12, 16}) {
     const int tpr = exact_tpr(nfrag, nv);
     if (tpr == 0 || tpr < EP_SM_TMA_MIN_TPR) continue;
     *rows_per_tile = kWsConsumers / tpr;
@@ -1040,8 +1034,20 @@ TmaRowFn pick_tma_row_kernel(int64_t cols, int* rows_per_tile, bool* halves) {
     // NV = 8 below TPR = 256 is NV = 4 at twice the TPR.  A 256x8 row is 32 KB:
     // staged in halves, so that two CTAs (three stages each) fit on an SM
     if (tpr == 256 && nv == 8) {
-      *halves = true;
-      return k_bias_softmax_rows_tma<T, 256, 8, true, true>;
+      *parts = 2;
+      return k_bias_softmax_rows_tma<T, 256, 8, true, 2>;
+    }
+    if constexpr (VW == 4) {
+      // float32 rows of 12288 and 16384: 48 and 64 floats a thread, staged in
+      // 16 KB parts
+      if (tpr == 256 && nv == 12) {
+        *parts = 3;
+        return k_bias_softmax_rows_tma<T, 256, 12, true, 3>;
+      }
+      if (tpr == 256 && nv == 16) {
+        *parts = 4;
+        return k_bias_softmax_rows_tma<T, 256, 16, true, 4>;
+      }
     }
     EP_SM_TMA_EXACT(4, 3)     // NV = 3 above TPR = 4 is NV = 6 at half the TPR; NV = 2 is never
                               // reached (nfrag = 2 TPR is NV = 4 at TPR / 2, or under 12 fragments)
@@ -1069,17 +1075,17 @@ template <typename T>
 bool launch_tma_rows(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_count, cudaStream_t stream,
                      int* launches, cudaError_t* err) {
   int rt = 0;
-  bool halves = false;
-  TmaRowFn f = pick_tma_row_kernel<T>(a.cols, &rt, &halves);
+  int parts = 1;
+  TmaRowFn f = pick_tma_row_kernel<T>(a.cols, &rt, &parts);
   if (f == nullptr) return false;
-  // a stage holds a tile (or with halves half a row) and its bias rows
-  const uint32_t row_bytes = uint32_t(a.cols * int64_t(sizeof(T))) / (halves ? 2u : 1u);
-  const int64_t slots = halves ? 1
+  // a stage holds a tile (or one part of a row) and its bias rows
+  const uint32_t row_bytes = uint32_t(a.cols * int64_t(sizeof(T))) / uint32_t(parts);
+  const int64_t slots = parts > 1 ? 1
                       : a.inner ? std::min<int64_t>(rt, (rt - 1) / a.inner_repeat + 2)
                                 : std::min<int64_t>(rt, a.bias_rows);
   const uint32_t stage_bytes = uint32_t(rt + slots) * row_bytes;
   if (2 * stage_bytes > 2 * kTmaStageBudget) return false;
-  const int stages = std::min<int>(kTmaMaxStages, std::max<int>(halves ? 3 : 2, kTmaStageBudget / stage_bytes));
+  const int stages = std::min<int>(kTmaMaxStages, std::max<int>(parts > 1 ? 3 : 2, kTmaStageBudget / stage_bytes));
   const size_t smem = size_t(stages) * stage_bytes;
   int per_sm = 1;
   *err = resident_ctas(reinterpret_cast<const void*>(f), kWsThreads, smem, &per_sm);
