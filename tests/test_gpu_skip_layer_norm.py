@@ -228,6 +228,7 @@ def test_workload_full_size_sampled_rows(lib, name):
     ("f32", 1024, 20001, None), ("f16", 4096, 6003, None), ("f32", 1024, 20000, 2000),
     ("f32", 768, 12007, 12007), ("f16", 2048, 9000, 3), ("f16", 512, 30001, 30001),
     ("f16", 32, 21000, 7), ("f32", 64, 9001, 9001), ("bf16", 128, 40000, 5),   # 64-row tiles
+    ("f16", 12288, 600, 3), ("f32", 12288, 401, 401), ("f32", 16384, 300, 4),   # 1-row tiles; f32 in parts
 ])
 def test_staged_many_tiles(lib, dtype, H, rows, skip_rows):
     if skip_rows is None or skip_rows == rows:
@@ -251,6 +252,7 @@ def test_staged_many_tiles(lib, dtype, H, rows, skip_rows):
 
 _EXACT_SHAPES = ([(t, nv) for nv in (3, 4, 5, 7) for t in (4, 8, 16, 32, 64, 128, 256)]
                  + [(256, 6), (256, 8), (4, 2), (4, 1)])
+_F32_PART_SHAPES = [(256, 12), (256, 16)]   # float32 rows staged in 3 and 4 parts
 _RAGGED_NFRAG = [40, 100, 200, 300, 700, 1500]   # 16x4, 32x4, 64x4, 128x4, 256x4, 256x8 with idle lanes
 
 
@@ -259,6 +261,7 @@ def _shape_cases():
     for dt, vw in (("f32", 4), ("f16", 8), ("bf16", 8)):
         out += [(dt, t * nv * vw) for t, nv in _EXACT_SHAPES]
         out += [(dt, nf * vw) for nf in _RAGGED_NFRAG]
+    out += [("f32", t * nv * 4) for t, nv in _F32_PART_SHAPES]
     return out
 
 

@@ -256,7 +256,7 @@ constexpr int kTmaMaxStages = 8;
 // Dynamic shared memory: [gamma | beta | bias] (each `param_stride` bytes,
 // beta/bias only when present), then the stages.  EXACT: the row is exactly
 // TPR*NV fragments, so no column needs a bounds check.
-template <typename T, int TPR, int NV, bool EXACT>
+template <typename T, int TPR, int NV, bool EXACT, int PARTS = 1>
 __global__ void __launch_bounds__(kWsThreads, EP_SLN_TMA_MIN_CTAS)
 k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_t param_stride) {
   constexpr int VW = dev::Vec16<T>::N;
@@ -271,13 +271,16 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
   __shared__ float red_a[kWsConsumerWarps];
   __shared__ float red_b[kWsConsumerWarps];
 
+  static_assert(PARTS == 1 || (RT == 1 && EXACT && NV % PARTS == 0), "parts: one exact row a tile");
   const int H = static_cast<int>(a.H);  // staged rows are at most 64 KB
-  const uint32_t row_bytes = static_cast<uint32_t>(H) * uint32_t(sizeof(T));
+  // a stage holds a tile of rows, or one part of a row (input, then skip)
+  const uint32_t row_bytes = static_cast<uint32_t>(H) * uint32_t(sizeof(T)) / uint32_t(PARTS);
   const uint32_t tile_bytes = RT * row_bytes;
   const uint32_t stage_bytes = 2 * tile_bytes;
   const bool has_beta = a.beta != nullptr;
   const bool has_bias = a.bias != nullptr;
-  const uint32_t param_bytes = param_stride * (1u + has_beta + has_bias);
+  // part-staged rows read gamma/beta/bias through the read-only path instead
+  const uint32_t param_bytes = PARTS > 1 ? 0u : param_stride * (1u + has_beta + has_bias);
   unsigned char* stage0 = smem + param_bytes;
   const int tid = threadIdx.x;
 
@@ -302,10 +305,14 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
     const T* sk = static_cast<const T*>(a.skip);
     const uint64_t pol_stream = dev::policy_evict_first();
     const uint64_t pol_keep = dev::policy_evict_last();
-    dev::mbar_arrive_expect_tx(&params_bar, param_bytes / param_stride * row_bytes);
-    dev::bulk_g2s(smem, a.gamma, row_bytes, &params_bar, pol_keep);
-    if (has_beta) dev::bulk_g2s(smem + param_stride, a.beta, row_bytes, &params_bar, pol_keep);
-    if (has_bias) dev::bulk_g2s(smem + param_stride * (1u + has_beta), a.bias, row_bytes, &params_bar, pol_keep);
+    if constexpr (PARTS > 1) {
+      dev::mbar_arrive(&params_bar);
+    } else {
+      dev::mbar_arrive_expect_tx(&params_bar, param_bytes / param_stride * row_bytes);
+      dev::bulk_g2s(smem, a.gamma, row_bytes, &params_bar, pol_keep);
+      if (has_beta) dev::bulk_g2s(smem + param_stride, a.beta, row_bytes, &params_bar, pol_keep);
+      if (has_bias) dev::bulk_g2s(smem + param_stride * (1u + has_beta), a.bias, row_bytes, &params_bar, pol_keep);
+    }
     // one CTA per tile: take over the tiles of cancelled CTAs; else round-robin
     const bool use_clc = EP_SLN_CLC && int64_t(gridDim.x) == ntiles;
     dev::ClcStream clc(&clc_resp, &clc_bar);
@@ -330,6 +337,31 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
       const int64_t r0 = tile * RT;
       const uint32_t nr = static_cast<uint32_t>(min(int64_t(RT), a.rows - r0));
       unsigned char* dst = stage0 + size_t(st) * stage_bytes;
+      if constexpr (PARTS > 1) {
+        // part p of the input row and of its skip row in the p-th stage from here
+        const int64_t sr = a.skip_bcast ? r0 % a.skip_rows : r0;
+        const int part_cols = H / PARTS;
+        for (int p = 0; p < PARTS; ++p) {
+          int sp = st;
+          if (p > 0) {
+            ++j;
+            ring.next();
+            sp = ring.st;
+            if (j >= stages && !dev::mbar_wait(&empty[sp], ring.phase ^ 1u)) {
+              for (int64_t k = j - stages; k < j; ++k)
+                dev::mbar_wait(&full[k % stages], static_cast<uint32_t>((k / stages) & 1));
+              clc.drain();
+              return;
+            }
+            tile_of[sp] = tile;
+          }
+          unsigned char* dp = stage0 + size_t(sp) * stage_bytes;
+          dev::mbar_arrive_expect_tx(&full[sp], 2u * row_bytes);
+          dev::bulk_g2s(dp, in + r0 * H + p * part_cols, row_bytes, &full[sp], pol_stream);
+          dev::bulk_g2s(dp + tile_bytes, sk + sr * H + p * part_cols, row_bytes, &full[sp],
+                        a.skip_bcast ? pol_keep : pol_stream);
+        }
+      } else {
       dev::mbar_arrive_expect_tx(&full[st], 2u * nr * row_bytes);
       dev::bulk_g2s(dst, in + r0 * H, nr * row_bytes, &full[st], pol_stream);
       if (!a.skip_bcast) {
@@ -340,6 +372,7 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
           dev::bulk_g2s(dst + tile_bytes + q * row_bytes, sk + sr * H, row_bytes, &full[st], pol_keep);
           if (++sr == a.skip_rows) sr = 0;
         }
+      }
       }
       if (use_clc) {
         tile = clc.next();
@@ -358,6 +391,17 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
   const T* p_gamma = reinterpret_cast<const T*>(smem);
   const T* p_beta = reinterpret_cast<const T*>(smem + param_stride);
   const T* p_bias = reinterpret_cast<const T*>(smem + param_stride * (1u + has_beta));
+  // a parameter fragment: from shared memory, or for part-staged rows from global
+  auto param = [&](const T* staged, const void* global, int c, float (&f)[VW]) {
+    if constexpr (PARTS > 1) {
+      dev::Frag<T, VW> q;
+      q.load_keep(static_cast<const T*>(global) + c);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) f[e] = q.v[e];
+    } else {
+      dev::lds_unpack(staged + c, f);
+    }
+  };
   const int g = tid / TPR;
   const int lane = tid % TPR;
   const int bar_id = 1 + g;            // named barrier of a multi-warp group
@@ -376,27 +420,53 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
 
     const int64_t r = tile * RT + g;
     const bool active = r < a.rows;
-    const unsigned char* stage = stage0 + size_t(st) * stage_bytes;
-    const T* s_in = reinterpret_cast<const T*>(stage) + g * H;
-    const T* s_sk = reinterpret_cast<const T*>(stage + tile_bytes) + g * H;
-
     float s[NV][VW];
+    if constexpr (PARTS > 1) {
+      // part p of the row (fragments [p PV, (p+1) PV)) is in the p-th stage
+      constexpr int PV = NV / PARTS;
+      const int part_cols = H / PARTS;
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      const int c = (v * TPR + lane) * VW;
-      if (active && (EXACT || c < H)) {
-        float k[VW];
-        dev::lds_unpack(s_in + c, s[v]);
-        dev::lds_unpack(s_sk + c, k);
+      for (int p = 0; p < PARTS; ++p) {
+        if (p > 0) {
+          ring.next();
+          if (!dev::named_barrier_and(bar_id, TPR, dev::mbar_wait(&full[ring.st], ring.phase))) return;
+        }
+        const unsigned char* stage = stage0 + size_t(ring.st) * stage_bytes;
+        const T* s_in = reinterpret_cast<const T*>(stage);
+        const T* s_sk = reinterpret_cast<const T*>(stage + tile_bytes);
 #pragma unroll
-        for (int e = 0; e < VW; ++e) s[v][e] = __fadd_rn(s[v][e], k[e]);
-      } else {
+        for (int v = p * PV; v < (p + 1) * PV; ++v) {
+          const int c = (v * TPR + lane) * VW - p * part_cols;
+          float k[VW];
+          dev::lds_unpack(s_in + c, s[v]);
+          dev::lds_unpack(s_sk + c, k);
 #pragma unroll
-        for (int e = 0; e < VW; ++e) s[v][e] = 0.f;
+          for (int e = 0; e < VW; ++e) s[v][e] = active ? __fadd_rn(s[v][e], k[e]) : 0.f;
+        }
+        __syncwarp();
+        if ((tid & 31) == 0) dev::mbar_arrive(&empty[ring.st]);
       }
+    } else {
+      const unsigned char* stage = stage0 + size_t(st) * stage_bytes;
+      const T* s_in = reinterpret_cast<const T*>(stage) + g * H;
+      const T* s_sk = reinterpret_cast<const T*>(stage + tile_bytes) + g * H;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int c = (v * TPR + lane) * VW;
+        if (active && (EXACT || c < H)) {
+          float k[VW];
+          dev::lds_unpack(s_in + c, s[v]);
+          dev::lds_unpack(s_sk + c, k);
+#pragma unroll
+          for (int e = 0; e < VW; ++e) s[v][e] = __fadd_rn(s[v][e], k[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < VW; ++e) s[v][e] = 0.f;
+        }
+      }
+      __syncwarp();
+      if ((tid & 31) == 0) dev::mbar_arrive(&empty[st]);
     }
-    __syncwarp();
-    if ((tid & 31) == 0) dev::mbar_arrive(&empty[st]);
 
     const int64_t off = r * H;
     if (active && (has_bias || sum_out != nullptr)) {
@@ -406,7 +476,7 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
         if (EXACT || c < H) {
           if (has_bias) {
             float b[VW];
-            dev::lds_unpack(p_bias + c, b);
+            param(p_bias, a.bias, c, b);
 #pragma unroll
             for (int e = 0; e < VW; ++e) s[v][e] = __fadd_rn(s[v][e], b[e]);
           }
@@ -446,10 +516,10 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
         const int c = (v * TPR + lane) * VW;
         if (EXACT || c < H) {
           float gm[VW], y[VW];
-          dev::lds_unpack(p_gamma + c, gm);
+          param(p_gamma, a.gamma, c, gm);
           if (has_beta) {
             float bt[VW];
-            dev::lds_unpack(p_beta + c, bt);
+            param(p_beta, a.beta, c, bt);
 #pragma unroll
             for (int e = 0; e < VW; ++e) y[e] = fmaf(s[v][e] * rstd, gm[e], bt[e]);
           } else {
@@ -530,15 +600,31 @@ inline int exact_tpr(int64_t nfrag, int nv) {
 }
 
 template <typename T>
-TmaFn pick_tma_kernel(int64_t H, int* rows_per_tile) {
+TmaFn pick_tma_kernel(int64_t H, int* rows_per_tile, int* parts) {
   constexpr int VW = dev::Vec16<T>::N;
   const int64_t nfrag = H / VW;
+  *parts = 1;
   if (nfrag < 4) return nullptr;
   // exact shapes; the compiled set is every (TPR, NV) this search can return
-  for (int nv : {3, 4, 5, 6, 7, 8, 2, 1}) {
+  for (int nv : {3, 4, 5, 6, 7, 8, 2, 1, 12, 16}) {
     const int tpr = exact_tpr(nfrag, nv);
     if (tpr == 0) continue;
     *rows_per_tile = kWsConsumers / tpr;
+    // float32 rows of 12288 and 16384 (48 and 64 floats a thread): staged in
+    // 16 KB parts, gamma/beta/bias read through the read-only path (whole rows
+    // of them would fill shared memory).  Measured at 256 MB: 0.62-0.69 of the
+    // copy bandwidth on the register kernel, 0.93-0.97 here.  (16-bit rows of
+    // 12288 in two parts measured no faster than whole rows.)
+    if constexpr (VW == 4) {
+      if (tpr == 256 && nv == 12) {
+        *parts = 3;
+        return k_skip_layer_norm_tma<T, 256, 12, true, 3>;
+      }
+      if (tpr == 256 && nv == 16) {
+        *parts = 4;
+        return k_skip_layer_norm_tma<T, 256, 16, true, 4>;
+      }
+    }
 #define EP_SLN_TMA_EXACT(TPR_, NV_) \
     if (tpr == TPR_ && nv == NV_) return k_skip_layer_norm_tma<T, TPR_, NV_, true>;
     EP_SLN_TMA_EXACT(4, 3) EP_SLN_TMA_EXACT(8, 3) EP_SLN_TMA_EXACT(16, 3) EP_SLN_TMA_EXACT(32, 3)
@@ -584,13 +670,13 @@ cudaError_t launch_t(const SlnArgs& a, int sm_count, cudaStream_t stream, int* l
   const bool vec = (a.H % VW == 0) && al16(a.input) && al16(a.skip) && al16(a.gamma) &&
                    al16(a.beta) && al16(a.bias) && al16(a.output) && al16(a.sum_out);
   if (vec && EP_SLN_TMA) {
-    int rt = 0;
-    if (TmaFn f = pick_tma_kernel<T>(a.H, &rt)) {
+    int rt = 0, parts = 1;
+    if (TmaFn f = pick_tma_kernel<T>(a.H, &rt, &parts)) {
       const uint32_t row_bytes = uint32_t(a.H * int64_t(sizeof(T)));
-      const uint32_t stage_bytes = 2u * uint32_t(rt) * row_bytes;
+      const uint32_t stage_bytes = 2u * uint32_t(rt) * row_bytes / uint32_t(parts);
       const uint32_t param_stride = (row_bytes + 127u) / 128u * 128u;
-      const uint32_t param_bytes = param_stride * (1u + (a.beta != nullptr) + (a.bias != nullptr));
-      const int stages = std::min<int>(kTmaMaxStages, std::max<int>(2, kTmaStageBudget / stage_bytes));
+      const uint32_t param_bytes = parts > 1 ? 0u : param_stride * (1u + (a.beta != nullptr) + (a.bias != nullptr));
+      const int stages = std::min<int>(kTmaMaxStages, std::max<int>(parts > 1 ? 3 : 2, kTmaStageBudget / stage_bytes));
       if (2 * stage_bytes <= 2 * kTmaStageBudget && param_bytes <= 96u * 1024u) {
         const size_t smem = param_bytes + size_t(stages) * stage_bytes;
         int per_sm = 1;
