@@ -173,7 +173,7 @@ def bias_softmax_dims(shape, bias_numel, axis=DEFAULT_AXIS):
     """`derive` block of the com.microsoft.BiasSoftmax manifest:
     axisNorm, batchCount (product of dims before axisNorm), blockSize (product
     from axisNorm on), biasBlockCount = numel(bias)/blockSize, innerRepeat =
-    batchCount / biasBlockCount, and the `biasContract` verdict."""
+    batchCount / biasBlockCount, and whether `biasContract` holds."""
     rank = len(shape)
     axis_n = axis if axis >= 0 else axis + rank
     if not (0 <= axis_n < rank):
