@@ -61,3 +61,21 @@ def test_reference_arm_runs_on_rank_zero_only():
     with contextlib.redirect_stdout(out):
         rc = bench.run_reference(args, ws=2, rank=1)
     assert rc == 0 and out.getvalue() == ""
+
+
+def test_reference_arm_prints_one_contract_line():
+    # rank 0 runs the oracle on bounded samples of the workloads and prints the
+    # same JSON line as the GPU arm, marked as the reference
+    import json
+    args = argparse.Namespace(steps=1, warmup=3, gpus=1)
+    out = io.StringIO()
+    with contextlib.redirect_stdout(out):
+        rc = bench.run_reference(args, ws=1, rank=0)
+    lines = [l for l in out.getvalue().splitlines() if l.strip()]
+    assert rc == 0 and len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "GB/s"
+    assert d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert "workload" in d["config"]
