@@ -72,16 +72,16 @@ ORDER = [
 # step serves from L2, and writes still dirty in L2 at a kernel's end are not
 # counted.)
 NCU_TRAFFIC = {
-    "sln_f16_16384x4096_bias_residual": 478105088,
-    "sln_f32_2x128x768": 1608192,
-    "sln_f32_32x2048x1024_bcast_skip": 487029504,
-    "bias_add_f16_16x1024x4096": 348322048,
-    "bias_softmax_f32_64x262144_cyclic": 153304832,
-    "quick_gelu_f16_67108867": 206551808,
-    "bias_softmax_f16_32x16x512x512_causal": 492431104,
-    "bias_softmax_f32_8x1048576": 75640064,
+    "sln_f16_16384x4096_bias_residual": 478330624,
+    "sln_f32_2x128x768": 1608448,
+    "sln_f32_32x2048x1024_bcast_skip": 485532160,
+    "bias_add_f16_16x1024x4096": 348293632,
+    "bias_softmax_f32_64x262144_cyclic": 153212672,
+    "quick_gelu_f16_67108867": 206419968,
+    "bias_softmax_f16_32x16x512x512_causal": 492419072,
+    "bias_softmax_f32_8x1048576": 75611392,
 }
-NCU_TRAFFIC_SOURCE_HASH = "cda6206e5acd4b0c"
+NCU_TRAFFIC_SOURCE_HASH = "1b5ebf76308820cf"
 
 
 def kernel_source_hash() -> str:

@@ -676,7 +676,13 @@ cudaError_t launch_t(const SlnArgs& a, int sm_count, cudaStream_t stream, int* l
       const uint32_t stage_bytes = 2u * uint32_t(rt) * row_bytes / uint32_t(parts);
       const uint32_t param_stride = (row_bytes + 127u) / 128u * 128u;
       const uint32_t param_bytes = parts > 1 ? 0u : param_stride * (1u + (a.beta != nullptr) + (a.bias != nullptr));
-      const int stages = std::min<int>(kTmaMaxStages, std::max<int>(parts > 1 ? 3 : 2, kTmaStageBudget / stage_bytes));
+      int stages = std::min<int>(kTmaMaxStages, std::max<int>(parts > 1 ? 3 : 2, kTmaStageBudget / stage_bytes));
+      // A CTA whose parameters and two stages already exceed half of shared
+      // memory runs alone on its SM: give it as many stages as fit, so that
+      // more rows are in flight (f16 H = 10240-12288, f32 H = 5120-6144).
+      constexpr uint32_t kSmemForStages = 224u * 1024u;
+      if (param_bytes + 2u * stage_bytes > kSmemForStages / 2 && param_bytes + 2u * stage_bytes <= kSmemForStages)
+        stages = std::min<int>(kTmaMaxStages, std::max<int>(stages, int((kSmemForStages - param_bytes) / stage_bytes)));
       if (2 * stage_bytes <= 2 * kTmaStageBudget && param_bytes <= 96u * 1024u) {
         const size_t smem = param_bytes + size_t(stages) * stage_bytes;
         int per_sm = 1;
