@@ -51,6 +51,21 @@ def test_binding_signatures_cover_the_header():
     assert set(declared_functions()) <= set(_binding._SIGNATURES)
 
 
+def test_binding_argument_counts_match_the_prototypes():
+    # a ctypes binding whose argument list drifts from the C prototype passes
+    # garbage silently; compare every declared function's parameter count
+    from transformer_epilogue_gb300 import _binding
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    protos = dict(re.findall(r"(ep_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", src, flags=re.S))
+    assert set(protos) == set(declared_functions())
+    for name, params in protos.items():
+        params = params.strip()
+        n = 0 if params in ("", "void") else len(params.split(","))
+        assert len(_binding._SIGNATURES[name][1]) == n, name
+
+
 def test_host_validation_contracts(built_lib):
     env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
     p = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "abi_host_cases.py")], env=env,
