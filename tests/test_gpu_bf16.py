@@ -1,6 +1,7 @@
 """bfloat16 through every op and kernel path: CUDA (through the C ABI) vs the
-float64 oracle, |gpu - o| <= one bfloat16 spacing at |o|; the residual output
-and bias-row indexing bit-exact."""
+float64 oracle, |gpu - o| <= half a bfloat16 spacing plus the float32 error
+bound of each op's arithmetic (tests/_helpers.py); the residual output and
+bias-row indexing bit-exact."""
 import numpy as np
 import pytest
 import torch
@@ -10,7 +11,6 @@ from gen import synth
 from tests import test_gpu_bias_softmax as sm
 from tests import test_gpu_elementwise as ew
 from tests import test_gpu_skip_layer_norm as sln
-from tests._helpers import assert_elementwise_close
 
 pytestmark = pytest.mark.gpu
 
@@ -65,14 +65,14 @@ def test_bias_softmax_bf16_causal(lib):
 def test_bias_add_bf16(lib, shape):
     d = synth.bias_add_inputs(shape, "bf16", seed=sum(shape))
     out = ew.run_bias_add(lib, d)
-    assert_elementwise_close(out, oracle.bias_add(d["X"], d["bias"], d["skip"]), torch.bfloat16)
+    ew.check_bias_add(out, d["X"], d["bias"], d["skip"])
 
 
 @pytest.mark.parametrize("n,offs", [(1001, None), ((1 << 20) + 5, None), (70000, {"X": 2, "Y": 2})])
 def test_quick_gelu_bf16(lib, n, offs):
     d = synth.quick_gelu_inputs(n, "bf16", seed=n)
     out = ew.run_gelu(lib, d["X"], d["alpha"], offsets=offs)
-    assert_elementwise_close(out, oracle.quick_gelu(d["X"], d["alpha"]), torch.bfloat16)
+    ew.check_quick_gelu(out, d["X"], d["alpha"])
 
 
 def test_quick_gelu_bf16_all_values(lib):
@@ -80,7 +80,7 @@ def test_quick_gelu_bf16_all_values(lib):
     x = bits.view(torch.bfloat16)
     x = x[torch.isfinite(x)].contiguous()
     out = ew.run_gelu(lib, x, 1.702)
-    assert_elementwise_close(out, oracle.quick_gelu(x, 1.702), torch.bfloat16)
+    ew.check_quick_gelu(out, x, 1.702)
 
 
 def test_bias_add_bf16_cancellation(lib):
@@ -91,7 +91,7 @@ def test_bias_add_bf16_cancellation(lib):
     b = torch.randn(64, generator=g).to(torch.bfloat16)
     s = (-(x.double() + b.double()) + torch.randn(4, 8, 64, generator=g).double() * 1e-2).to(torch.bfloat16)
     out = ew.run_bias_add(lib, dict(X=x, bias=b, skip=s))
-    assert_elementwise_close(out, oracle.bias_add(x, b, s), torch.bfloat16)
+    ew.check_bias_add(out, x, b, s)
 
 
 @pytest.mark.parametrize("mode", ["skip_is_minus_x", "skip_is_minus_bias", "random"])
@@ -116,4 +116,4 @@ def test_bias_add_bf16_wide_exponents(lib, mode):
     else:
         s = wide(4, 64, 64)
     out = ew.run_bias_add(lib, dict(X=x, bias=b, skip=s))
-    assert_elementwise_close(out, oracle.bias_add(x, b, s), torch.bfloat16)
+    ew.check_bias_add(out, x, b, s)

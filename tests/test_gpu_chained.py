@@ -13,7 +13,8 @@ import torch
 
 import oracle
 from gen import synth
-from tests._helpers import assert_elementwise_close, assert_norm_close
+from tests import test_gpu_elementwise as ew
+from tests._helpers import assert_norm_close
 
 pytestmark = pytest.mark.gpu
 
@@ -41,8 +42,8 @@ def test_read_after_write_chain(lib, dtype):
     o1, o2, o3, o4 = (t.cpu() for t in (out1, out2, out3, out4))
     assert_norm_close(o1, oracle.skip_layer_norm(d["input"], d["skip"], d["gamma"], d["beta"], d["bias"],
                                                  d["epsilon"])["output"], T)
-    assert_elementwise_close(o2, oracle.quick_gelu(o1, 1.702), T)
-    assert_elementwise_close(o3, oracle.bias_add(o2.view(1, R, H), ba["bias"], ba["skip"]).reshape(R, H), T)
+    ew.check_quick_gelu(o2, o1, 1.702)
+    ew.check_bias_add(o3.view(1, R, H), o2.view(1, R, H), ba["bias"], ba["skip"])
     assert_norm_close(o4, oracle.bias_softmax(o3, sm["bias"], axis=1, is_inner_broadcast=0), T)
 
 
@@ -60,7 +61,7 @@ def test_write_after_read(lib):
     lib.ep_skip_layer_norm(d["input"].cuda(), d["skip"].cuda(), d["gamma"].cuda(), d["beta"].cuda(), None,
                            d["epsilon"], output=P.view(R, H))             # and again
     torch.cuda.synchronize()
-    assert_elementwise_close(Q.cpu(), oracle.quick_gelu(p0, 1.702), torch.float16)
+    ew.check_quick_gelu(Q.cpu(), p0, 1.702)
     assert_norm_close(P.view(R, H).cpu(), oracle.skip_layer_norm(d["input"], d["skip"], d["gamma"], d["beta"], None,
                                                                  d["epsilon"])["output"], torch.float16)
 
@@ -82,7 +83,7 @@ def test_split_softmax_after_producer(lib):
     torch.cuda.synchronize()
     z1 = torch.from_numpy(oracle.quick_gelu(q, 1.702)).float()
     assert_norm_close(y.cpu(), oracle.bias_softmax(z1, b, axis=1, is_inner_broadcast=0), torch.float32)
-    assert_elementwise_close(z.cpu(), oracle.quick_gelu(q, -1.0), torch.float32)
+    ew.check_quick_gelu(z.cpu(), q, -1.0)
 
 
 def test_two_streams_at_once(lib):

@@ -4,39 +4,74 @@ at start-up, code inside an allocator callback, or a loop that cannot afford
 the synchronisation cudaMalloc may cause).  Its split-row scratch is a fixed
 array inside the library instead of a caller-provided workspace.
 
-Two calls in a row, on different shapes, must each match the workspace entry
-point ep_bias_softmax within the usual BiasSoftmax tolerance; the second call
-runs on scratch still holding the first call's statistics.  (Shapes beyond
-the fixed scratch are rejected before anything is enqueued; that host-side
-check is covered without a GPU in tests/abi_host_cases.py.)  This file is
-collected last so that a failure here comes after every other test has run.
+Calls in a row, on different shapes, must each match the float64 oracle
+within the usual BiasSoftmax tolerance and equal the workspace entry point
+ep_bias_softmax bit for bit (the same kernels run on the same launch plan);
+every call after the first runs on scratch still holding the previous call's
+statistics.  The cases cover both split-row kernel pairs: the staged pair
+(16-byte-aligned rows) and the register pair (a row length that is not a
+multiple of the 16-byte vector, and a data pointer one element off).  Free
+device memory must not shrink across the calls.  (Shapes beyond the fixed
+scratch are rejected before anything is enqueued; that host-side check is
+covered without a GPU in tests/abi_host_cases.py.)  This file is collected
+last so that a failure here comes after every other test has run.
 """
 import pytest
 import torch
 
+import oracle
 from gen import synth
-from tests._helpers import assert_norm_close, to_np64
+from tests._helpers import assert_norm_close, offset_copy, to_np64
 
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # (data shape, bias shape, dtype, is_inner_broadcast): both take the split-row path
-    ((64, 1, 262144), (2, 1, 262144), "f32", 0),
-    ((6, 40000), (3, 40000), "f16", 1),
+    # (data shape, bias shape, dtype, is_inner_broadcast, data offset in bytes)
+    ((64, 1, 262144), (2, 1, 262144), "f32", 0, 0),   # staged pair, 4096 (max, sum) entries
+    ((6, 40000), (3, 40000), "f16", 1, 0),            # staged pair, ragged last chunk
+    ((5, 30001), (5, 30001), "f32", 0, 0),            # register pair: 30001 % 4 != 0
+    ((3, 50000), (1, 50000), "f16", 1, 2),            # register pair: data one element off
 ]
 
 
-def test_noalloc_matches_workspace_entry_point_twice(lib):
-    for data_shape, bias_shape, dtype, inner in CASES:
-        d = synth.bias_softmax_inputs(data_shape, bias_shape, dtype, data_std=2.0, seed=len(data_shape))
-        assert lib.ep_bias_softmax_workspace_size(d["data"].dtype, data_shape, 1) > 0
-        data, bias = d["data"].cuda(), d["bias"].cuda()
-        want = lib.ep_bias_softmax(data, bias, axis=1, is_inner_broadcast=inner)
-        got = torch.full_like(data, float("nan"))
-        n0 = lib.kernel_launch_count()
-        lib.ep_bias_softmax_noalloc(data, bias, axis=1, is_inner_broadcast=inner, output=got)
-        torch.cuda.synchronize()
-        assert lib.kernel_launch_count() > n0
-        rows = data.numel() // data_shape[-1]
-        assert_norm_close(got.reshape(rows, -1), to_np64(want.reshape(rows, -1)), data.dtype)
+def _call_pair(lib, data, bias, inner):
+    want = lib.ep_bias_softmax(data, bias, axis=1, is_inner_broadcast=inner)
+    got = torch.full_like(data, float("nan"))
+    n0 = lib.kernel_launch_count()
+    lib.ep_bias_softmax_noalloc(data, bias, axis=1, is_inner_broadcast=inner, output=got)
+    torch.cuda.synchronize()
+    assert lib.kernel_launch_count() > n0
+    return got, want
 
+
+def test_noalloc_matches_oracle_and_workspace_entry_point(lib):
+    mem0 = None
+    for rep in range(2):
+        if rep == 1:
+            # every kernel has run once and the first call has looked up the
+            # scratch array's address: from here on, device memory taken by
+            # anything other than PyTorch's own allocator would show as a drop
+            # in free memory beyond what PyTorch reserves
+            torch.cuda.synchronize()
+            mem0 = (torch.cuda.mem_get_info()[0], torch.cuda.memory_reserved())
+        for data_shape, bias_shape, dtype, inner, off in CASES:
+            d = synth.bias_softmax_inputs(data_shape, bias_shape, dtype, data_std=2.0,
+                                          seed=len(data_shape) + data_shape[-1])
+            assert lib.ep_bias_softmax_workspace_size(d["data"].dtype, data_shape, 1) > 0
+            keep = None
+            if off:
+                keep, data = offset_copy(d["data"], off)
+            else:
+                data = d["data"].cuda()
+            bias = d["bias"].cuda()
+            got, want = _call_pair(lib, data, bias, inner)
+            rows = data.numel() // data_shape[-1]
+            g2 = got.reshape(rows, -1).cpu()
+            assert_norm_close(g2, to_np64(want.reshape(rows, -1)), data.dtype)
+            assert torch.equal(got, want), f"{data_shape} {dtype}: differs from the workspace entry point"
+            o = oracle.bias_softmax(d["data"], d["bias"], axis=1, is_inner_broadcast=inner)
+            assert_norm_close(g2, o, data.dtype)
+            del keep, got, want, data, bias
+    torch.cuda.synchronize()
+    free1, reserved1 = torch.cuda.mem_get_info()[0], torch.cuda.memory_reserved()
+    assert free1 >= mem0[0] + mem0[1] - reserved1 - (2 << 20)
