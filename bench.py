@@ -10,8 +10,12 @@ value        = minimum bytes of all ops (every input read once, every output
                (every 8th timed step carries one event pair, around the dominant
                op; an event record costs ~2 us of stream time and ends the
                programmatic overlap of the kernels on either side)
-ops          = per-op means from a separate loop with an event pair around
-               every op
+ops          = per op: the mean from a separate loop of steps with an event pair
+               around every op ("in the step": each op also writes back the
+               previous op's dirty L2 lines), and the median / minimum / mean of
+               50 launches of the op alone, each after an L2 flush that leaves
+               only clean lines ("isolated"); fractions against the measured
+               copy bandwidth and against the nominal 8 TB/s
 e2e          = the same metric with each step's inputs copied host->device from
                pinned memory and outputs copied back, inside the timed region
 roofline     = the dominant kernel's algorithmic bytes / its mean CUDA-event
@@ -48,9 +52,11 @@ from gen import synth  # noqa: E402
 METRIC = "achieved HBM GB/s per op and % of GB300 HBM roofline; rows/sec for SkipLayerNorm"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
 
 # Step order: each small workload follows a large streaming one.
 K_BREAKDOWN = 50  # steps of the per-op breakdown loop
+K_ISOLATED = 50   # launches of each op alone, each after an L2 flush
 DOM_EVERY = 8     # timed steps per event-bracketed launch of the dominant op
 
 ORDER = [
@@ -64,22 +70,22 @@ ORDER = [
     "bias_softmax_f32_8x1048576",
 ]
 
-# DRAM bytes (read + write) per launch from ncu captures, keyed by workload,
-# with the hash of the kernel sources they were taken on.  A changed source
-# makes the figure stale and it is reported as null.
-# (profiles/dram_traffic_bench_kernels.md; ncu flushes L2 before each launch,
-# so the split-row softmax figures include a pass-2 re-read from DRAM that a
-# step serves from L2, and writes still dirty in L2 at a kernel's end are not
-# counted.)
+# DRAM bytes (read + write) per launch from ncu captures of each kernel alone
+# (`--profile NAME`: one workload, a few launches), keyed by workload, with the
+# hash of the kernel sources they were taken on.  A changed source makes the
+# figure stale and it is reported as null.  ncu flushes L2 before each launch,
+# so reads are cold (the split-row softmax: pass 2 re-reads from DRAM what a
+# step serves from L2), and writes still dirty in L2 when a kernel ends are not
+# counted.
 NCU_TRAFFIC = {
-    "sln_f16_16384x4096_bias_residual": 478330624,
-    "sln_f32_2x128x768": 1608448,
-    "sln_f32_32x2048x1024_bcast_skip": 485532160,
-    "bias_add_f16_16x1024x4096": 348293632,
-    "bias_softmax_f32_64x262144_cyclic": 153212672,
-    "quick_gelu_f16_67108867": 206419968,
-    "bias_softmax_f16_32x16x512x512_causal": 492419072,
-    "bias_softmax_f32_8x1048576": 75611392,
+    "bias_add_f16_16x1024x4096": 347462144,
+    "bias_softmax_f16_32x16x512x512_causal": 492603136,
+    "bias_softmax_f32_64x262144_cyclic": 153057536,
+    "bias_softmax_f32_8x1048576": 75628032,
+    "quick_gelu_f16_67108867": 207092736,
+    "sln_f16_16384x4096_bias_residual": 476619776,
+    "sln_f32_2x128x768": 1610240,
+    "sln_f32_32x2048x1024_bcast_skip": 487019520,
 }
 NCU_TRAFFIC_SOURCE_HASH = "1b5ebf76308820cf"
 
@@ -375,6 +381,32 @@ def sliced_workload(name, batch):
             for k, v in d.items()}
 
 
+def isolated_times(work, device, reps=K_ISOLATED):
+    """Each op alone, `reps` launches, each after an L2 flush outside the event
+    pair: write 2x L2 then read 2x L2, so the L2 holds only clean lines when
+    the op starts.  Returns per-op lists of durations (ms)."""
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 0) or (132 << 20))
+    fw = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+    fr = torch.ones(2 * l2 // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    out = []
+    for w in work:
+        ts = []
+        for _ in range(reps):
+            fw.zero_()
+            fr.max()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            w.call()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        out.append(ts)
+    del fw, fr
+    return out
+
+
 def run_profile(args):
     """Runs one workload `--reps` times and nothing else (a target for ncu)."""
     import transformer_epilogue_gb300 as te
@@ -480,6 +512,7 @@ def main(argv=None):
     torch.cuda.synchronize()
     per_op_ms = [statistics.fmean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(B)) for i in range(len(work))]
     dom = max(range(len(ORDER)), key=lambda i: per_op_ms[i])
+    iso_ms = isolated_times(work, device)
 
     # timed region: K steps; an event pair around the dominant op in every
     # DOM_EVERY-th step (its launch duration for the roofline), no other per-op
@@ -597,9 +630,15 @@ def main(argv=None):
     peak, peak_src = measured_peak()
     value = units / (total_ms / 1e3) / 1e9
     ops = {}
-    for n, b, ms in zip(ORDER, bytes_per, per_op_ms):
+    for n, b, ms, iso in zip(ORDER, bytes_per, per_op_ms, iso_ms):
         gbs = b / (ms / 1e3) / 1e9
-        o = {"us": ms * 1e3, "min_bytes": b, "gbs": gbs, "frac_of_measured_peak": gbs / peak}
+        med, mn = statistics.median(iso), min(iso)
+        o = {"us": ms * 1e3, "min_bytes": b, "gbs": gbs, "frac_of_measured_peak": gbs / peak,
+             "frac_nominal": gbs / NOMINAL_HBM_GBS,
+             "median_us": med * 1e3, "min_us": mn * 1e3, "mean_us": statistics.fmean(iso) * 1e3,
+             "isolated_gbs": b / (med / 1e3) / 1e9,
+             "isolated_frac_of_measured_peak": b / (med / 1e3) / 1e9 / peak,
+             "isolated_frac_nominal": b / (med / 1e3) / 1e9 / NOMINAL_HBM_GBS}
         r = rows_of(n, hosts[n])
         if r:
             o["rows_per_s"] = r / (ms / 1e3)
@@ -616,10 +655,15 @@ def main(argv=None):
                    "step_min_bytes": step_bytes, "l2": "inputs larger than L2 (2.8 GB per step; each op "
                    "streams buffers disjoint from the previous op's)", "parallelism": f"replicas x{ws}"},
         "frac_of_measured_peak": value / peak,
+        "frac_nominal": value / NOMINAL_HBM_GBS,
         "ops": ops,
-        "ops_timing": f"separate loop of {B} steps, an event pair around every op (each record adds ~2 us)",
+        "ops_timing": f"us/gbs/frac_*: in the step, separate loop of {B} steps with an event pair around every "
+                      f"op (each record adds ~2 us); median_us/min_us/mean_us/isolated_*: {K_ISOLATED} launches "
+                      f"of the op alone, each after an L2 flush leaving only clean lines (event resolution "
+                      f"quantises median and minimum)",
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
+                     "frac": achieved / peak, "frac_nominal": achieved / NOMINAL_HBM_GBS, "traffic": traffic,
+                     "peak_source": peak_src,
                      "duration_us": dom_ms * 1e3,
                      "duration_source": f"event pair around the op in every {DOM_EVERY}th timed step "
                                         f"({len(dom_steps)} launches), mean"},
