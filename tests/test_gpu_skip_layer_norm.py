@@ -357,3 +357,48 @@ def test_ex_default_matches_plain_entry_point(lib):
     a, s_a = run(lib, d, residual=True)
     b, s_b, _, _ = run_ex(lib, d, simplified=False)
     assert torch.equal(a, b) and torch.equal(s_a, s_b)
+
+
+# ---------------------------------------------------------------------------
+# rows of 16385-32768 elements that 512 threads cover exactly: the staged
+# kernel with 512 consumer threads, the row staged in parts; many rows so
+# that tiles are taken over by running CTAs and the stage ring wraps
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,H", [("f16", 20480), ("f16", 24576), ("f16", 28672), ("f16", 32768),
+                                     ("bf16", 20480), ("bf16", 32768),
+                                     ("f32", 18432), ("f32", 20480), ("f32", 22528), ("f32", 24576),
+                                     ("f32", 26624), ("f32", 28672), ("f32", 30720), ("f32", 32768)])
+def test_wide_rows_staged(lib, dtype, H):
+    rows = 331
+    d = synth.sln_inputs((rows, H), None, dtype, has_beta=True, has_bias=True, seed=H)
+    out, s = run(lib, d, residual=True)
+    check(d, out, s)
+
+
+@pytest.mark.parametrize("dtype,H,beta,bias,res,skip_rows", [
+    ("f16", 32768, False, False, False, None), ("f32", 20480, True, False, False, 5),
+    ("bf16", 24576, False, True, True, 7), ("f32", 32768, True, True, True, None),
+])
+def test_wide_rows_optional_inputs_and_broadcast_skip(lib, dtype, H, beta, bias, res, skip_rows):
+    rows = 161
+    if skip_rows is None:
+        d = synth.sln_inputs((rows, H), None, dtype, has_beta=beta, has_bias=bias, seed=H + 1)
+    else:
+        d = synth.sln_inputs((rows // skip_rows, skip_rows, H), (1, skip_rows, H), dtype, has_beta=beta,
+                             has_bias=bias, seed=H + 1)
+    out, s = run(lib, d, residual=res)
+    check(d, out, s)
+
+
+@pytest.mark.parametrize("simplified", [False, True])
+@pytest.mark.parametrize("dtype,H", [("f16", 28672), ("f32", 26624)])
+def test_wide_rows_ex_statistics(lib, simplified, dtype, H):
+    d = synth.sln_inputs((97, H), None, dtype, has_beta=not simplified, has_bias=True, seed=H + 2)
+    out, s, mean, inv = run_ex(lib, d, simplified)
+    o = oracle.skip_layer_norm(d["input"], d["skip"], d["gamma"], d["beta"], d["bias"], d["epsilon"],
+                               simplified=simplified)
+    assert_norm_close(out.reshape(-1, H), o["output"], d["input"].dtype)
+    assert_bit_exact(s.reshape(-1, H), oracle.skip_bias_sum(d["input"], d["skip"], d["bias"]))
+    np.testing.assert_allclose(mean.numpy().astype(np.float64), o["mean"], rtol=2e-5, atol=2e-6)
+    np.testing.assert_allclose(inv.numpy().astype(np.float64), o["inv_std_dev"], rtol=2e-5, atol=0)

@@ -232,8 +232,8 @@ __global__ void __launch_bounds__(1024) k_skip_layer_norm_long(const SlnKernelAr
 // Shared-memory-staged, warp-specialised kernel (the fast path for 16-byte-
 // aligned rows).
 //
-// A CTA has kWsConsumers consumer threads in row groups of TPR and one
-// producer warp.  Tiles are RT = kWsConsumers/TPR consecutive rows; each of the
+// A CTA has NC consumer threads (256; 512 for the widest rows) in row groups
+// of TPR and one producer warp.  Tiles are RT = NC/TPR consecutive rows; each of the
 // `stages` shared-memory stages holds one tile: the RT input rows, then the RT
 // skip rows (for a broadcast skip, rows r mod skipRows), and the stage header
 // names the tile (-1: no more work).  Per stage, `full` completes when the
@@ -249,18 +249,17 @@ __global__ void __launch_bounds__(1024) k_skip_layer_norm_long(const SlnKernelAr
 // ---------------------------------------------------------------------------
 
 constexpr int kWsConsumers = 256;
-constexpr int kWsThreads = kWsConsumers + 32;
-constexpr int kWsConsumerWarps = kWsConsumers / 32;
 constexpr int kTmaMaxStages = 8;
 
 // Dynamic shared memory: [gamma | beta | bias] (each `param_stride` bytes,
 // beta/bias only when present), then the stages.  EXACT: the row is exactly
 // TPR*NV fragments, so no column needs a bounds check.
-template <typename T, int TPR, int NV, bool EXACT, int PARTS = 1>
-__global__ void __launch_bounds__(kWsThreads, EP_SLN_TMA_MIN_CTAS)
+template <typename T, int TPR, int NV, bool EXACT, int PARTS = 1, int NC = kWsConsumers>
+__global__ void __launch_bounds__(NC + 32, NC > kWsConsumers ? 1 : EP_SLN_TMA_MIN_CTAS)
 k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_t param_stride) {
   constexpr int VW = dev::Vec16<T>::N;
-  constexpr int RT = kWsConsumers / TPR;
+  constexpr int RT = NC / TPR;
+  constexpr int NCW = NC / 32;  // consumer warps
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[kTmaMaxStages];
   __shared__ __align__(8) uint64_t empty[kTmaMaxStages];
@@ -268,8 +267,8 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
   __shared__ __align__(8) uint64_t clc_bar;
   __shared__ __align__(16) uint4 clc_resp;
   __shared__ int64_t tile_of[kTmaMaxStages];  // stage header: the tile, or -1
-  __shared__ float red_a[kWsConsumerWarps];
-  __shared__ float red_b[kWsConsumerWarps];
+  __shared__ float red_a[NCW];
+  __shared__ float red_b[NCW];
 
   static_assert(PARTS == 1 || (RT == 1 && EXACT && NV % PARTS == 0), "parts: one exact row a tile");
   const int H = static_cast<int>(a.H);  // staged rows are at most 64 KB
@@ -287,7 +286,7 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
   if (tid == 0) {
     for (int st = 0; st < stages; ++st) {
       dev::mbar_init(&full[st], 1);
-      dev::mbar_init(&empty[st], kWsConsumerWarps);
+      dev::mbar_init(&empty[st], NCW);
     }
     dev::mbar_init(&params_bar, 1);
     dev::mbar_init(&clc_bar, 1);
@@ -298,9 +297,9 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
   dev::pdl_trigger();
   if (int64_t(blockIdx.x) >= ntiles) return;
 
-  if (tid >= kWsConsumers) {
+  if (tid >= NC) {
     // ---- producer: one thread issues every copy of this CTA ----
-    if (tid != kWsConsumers) return;
+    if (tid != NC) return;
     const T* in = static_cast<const T*>(a.input);
     const T* sk = static_cast<const T*>(a.skip);
     const uint64_t pol_stream = dev::policy_evict_first();
@@ -599,12 +598,60 @@ inline int exact_tpr(int64_t nfrag, int nv) {
   return (t >= 4 && t <= 256 && (t & (t - 1)) == 0) ? static_cast<int>(t) : 0;
 }
 
+// Rows of 16385-32768 elements that 512 threads cover exactly (16-bit rows of
+// 20480, 24576, 28672 and 32768; float32 rows of every multiple of 2048): one
+// row a tile on 512 consumer threads holding NV fragments each (40-64 floats),
+// staged in NV/2 parts of 16 KB (NV odd: NV parts of 8 KB), gamma/beta/bias
+// through the read-only path; the CTA runs alone on its SM and takes as many
+// stages as fit, so the next row streams in while the consumers reduce and
+// write this one.
+constexpr int kWideTpr = 512;
+template <typename T, int NV>
+TmaFn wide_kernel() {
+  return k_skip_layer_norm_tma<T, kWideTpr, NV, true, (NV % 2 == 0 ? NV / 2 : NV), kWideTpr>;
+}
+
 template <typename T>
-TmaFn pick_tma_kernel(int64_t H, int* rows_per_tile, int* parts) {
+TmaFn pick_wide_kernel(int64_t nfrag, int* parts) {
+  constexpr int VW = dev::Vec16<T>::N;
+  if (nfrag % kWideTpr != 0) return nullptr;
+  const int64_t nv = nfrag / kWideTpr;
+  *parts = static_cast<int>(nv % 2 == 0 ? nv / 2 : nv);
+  if constexpr (VW == 8) {
+    switch (nv) {
+      case 5: return wide_kernel<T, 5>();
+      case 6: return wide_kernel<T, 6>();
+      case 7: return wide_kernel<T, 7>();
+      case 8: return wide_kernel<T, 8>();
+      default: return nullptr;
+    }
+  } else {
+    switch (nv) {
+      case 9: return wide_kernel<T, 9>();
+      case 10: return wide_kernel<T, 10>();
+      case 11: return wide_kernel<T, 11>();
+      case 12: return wide_kernel<T, 12>();
+      case 13: return wide_kernel<T, 13>();
+      case 14: return wide_kernel<T, 14>();
+      case 15: return wide_kernel<T, 15>();
+      case 16: return wide_kernel<T, 16>();
+      default: return nullptr;
+    }
+  }
+}
+
+template <typename T>
+TmaFn pick_tma_kernel(int64_t H, int* rows_per_tile, int* parts, int* consumers) {
   constexpr int VW = dev::Vec16<T>::N;
   const int64_t nfrag = H / VW;
   *parts = 1;
+  *consumers = kWsConsumers;
   if (nfrag < 4) return nullptr;
+  if (EP_SLN_WIDE && H > 16384) {
+    *rows_per_tile = 1;
+    *consumers = kWideTpr;
+    return pick_wide_kernel<T>(nfrag, parts);
+  }
   // exact shapes; the compiled set is every (TPR, NV) this search can return
   for (int nv : {3, 4, 5, 6, 7, 8, 2, 1, 12, 16}) {
     const int tpr = exact_tpr(nfrag, nv);
@@ -670,29 +717,34 @@ cudaError_t launch_t(const SlnArgs& a, int sm_count, cudaStream_t stream, int* l
   const bool vec = (a.H % VW == 0) && al16(a.input) && al16(a.skip) && al16(a.gamma) &&
                    al16(a.beta) && al16(a.bias) && al16(a.output) && al16(a.sum_out);
   if (vec && EP_SLN_TMA) {
-    int rt = 0, parts = 1;
-    if (TmaFn f = pick_tma_kernel<T>(a.H, &rt, &parts)) {
+    int rt = 0, parts = 1, consumers = kWsConsumers;
+    if (TmaFn f = pick_tma_kernel<T>(a.H, &rt, &parts, &consumers)) {
       const uint32_t row_bytes = uint32_t(a.H * int64_t(sizeof(T)));
       const uint32_t stage_bytes = 2u * uint32_t(rt) * row_bytes / uint32_t(parts);
       const uint32_t param_stride = (row_bytes + 127u) / 128u * 128u;
       const uint32_t param_bytes = parts > 1 ? 0u : param_stride * (1u + (a.beta != nullptr) + (a.bias != nullptr));
       int stages = std::min<int>(kTmaMaxStages, std::max<int>(parts > 1 ? 3 : 2, kTmaStageBudget / stage_bytes));
       // A CTA whose parameters and two stages already exceed half of shared
-      // memory runs alone on its SM: give it as many stages as fit, so that
-      // more rows are in flight (f16 H = 10240-12288, f32 H = 5120-6144).
+      // memory, or whose threads fill the register file, runs alone on its SM:
+      // give it as many stages as fit, so that more rows are in flight (f16
+      // H = 10240-12288, f32 H = 5120-6144, and the 512-thread wide rows).
       constexpr uint32_t kSmemForStages = 224u * 1024u;
-      if (param_bytes + 2u * stage_bytes > kSmemForStages / 2 && param_bytes + 2u * stage_bytes <= kSmemForStages)
+      const bool alone = consumers > kWsConsumers ||
+                         (param_bytes + 2u * stage_bytes > kSmemForStages / 2 &&
+                          param_bytes + 2u * stage_bytes <= kSmemForStages);
+      if (alone)
         stages = std::min<int>(kTmaMaxStages, std::max<int>(stages, int((kSmemForStages - param_bytes) / stage_bytes)));
       if (2 * stage_bytes <= 2 * kTmaStageBudget && param_bytes <= 96u * 1024u) {
         const size_t smem = param_bytes + size_t(stages) * stage_bytes;
+        const int threads = consumers + 32;
         int per_sm = 1;
-        cudaError_t e = resident_ctas(reinterpret_cast<const void*>(f), kWsThreads, smem, &per_sm);
+        cudaError_t e = resident_ctas(reinterpret_cast<const void*>(f), threads, smem, &per_sm);
         if (e != cudaSuccess) return e;
         const int64_t ntiles = (a.rows + rt - 1) / rt;
         // one CTA per tile under launch control, else a persistent grid
         const bool clc = EP_SLN_CLC && ntiles <= int64_t(INT32_MAX);
         const unsigned grid = static_cast<unsigned>(clc ? ntiles : std::min<int64_t>(ntiles, int64_t(sm_count) * per_sm));
-        e = launch(f, dim3(grid), dim3(kWsThreads), smem, stream, k, stages, ntiles, param_stride);
+        e = launch(f, dim3(grid), dim3(threads), smem, stream, k, stages, ntiles, param_stride);
         if (e == cudaSuccess) *launches += 1;
         return e;
       }

@@ -30,6 +30,11 @@
 #ifndef EP_SLN_TMA
 #define EP_SLN_TMA 1
 #endif
+// 1: rows of 16385-32768 elements that 512 threads cover exactly take the
+// staged kernel with 512 consumer threads (0: the 1024-thread register rows).
+#ifndef EP_SLN_WIDE
+#define EP_SLN_WIDE 1
+#endif
 // 1: one CTA per tile, running CTAs take over the tiles of CTAs they cancel
 // (cluster launch control); 0: persistent grid, tiles round-robin.
 #ifndef EP_SLN_CLC
