@@ -317,3 +317,42 @@ def test_packed_rows_bias_map_bit_exact(lib):
         want = torch.zeros(rows, cols)
         want[torch.arange(rows), torch.from_numpy(br)] = 1.0
         assert torch.equal(out, want)
+
+
+# ---------------------------------------------------------------------------
+# rows of 16385-32768 columns that 512 threads cover exactly: the staged row
+# kernel with 512 consumer threads, the row and its bias row staged in parts
+# ---------------------------------------------------------------------------
+
+_WIDE = [("f16", 20480), ("f16", 24576), ("f16", 28672), ("f16", 32768), ("bf16", 20480), ("bf16", 32768),
+         ("f32", 18432), ("f32", 20480), ("f32", 22528), ("f32", 24576), ("f32", 26624), ("f32", 28672),
+         ("f32", 30720), ("f32", 32768)]
+
+
+@pytest.mark.parametrize("dtype,cols", _WIDE)
+def test_wide_rows_staged(lib, dtype, cols):
+    rows, bias_rows = 301, 7
+    d = synth.bias_softmax_inputs((rows, cols), (bias_rows, cols), dtype, data_std=2.0, seed=cols)
+    for inner in (0, 1):
+        out = run(lib, d["data"], d["bias"], 1, inner)
+        check(d["data"], d["bias"], 1, inner, out)
+
+
+@pytest.mark.parametrize("dtype,cols", [("f16", 32768), ("f32", 20480)])
+def test_wide_rows_masked_and_in_place(lib, dtype, cols):
+    rows = 40
+    d = synth.bias_softmax_inputs((rows, cols), (rows, cols), dtype, data_std=2.0, seed=cols + 1)
+    data = d["data"].clone()
+    for r in range(0, rows, 3):
+        data[r, :cols // 3] = -float("inf")          # whole parts masked
+    for r in range(1, rows, 5):
+        data[r, cols - 4097:] = -float("inf")
+    data[rows // 2, :] = -float("inf")               # a fully masked row: NaN
+    out = run(lib, data, d["bias"], 1, 0)
+    live = [r for r in range(rows) if r != rows // 2]
+    check(data, d["bias"], 1, 0, out, rows=live)
+    assert torch.isnan(out[rows // 2]).all()
+    x = data.cuda()
+    lib.ep_bias_softmax(x, d["bias"].cuda(), axis=1, is_inner_broadcast=0, output=x)
+    torch.cuda.synchronize()
+    assert torch.equal(x.cpu()[live], out[live])

@@ -192,8 +192,8 @@ __global__ void __launch_bounds__(256) k_bias_softmax_packed(const SmKernelArgs 
 // Shared-memory-staged, warp-specialised row kernel (the fast path for
 // 16-byte-aligned rows).
 //
-// A CTA has kWsConsumers consumer threads in row groups of TPR and one
-// producer warp.  Tiles are RT = kWsConsumers/TPR consecutive data rows.  A
+// A CTA has NC consumer threads (256; 512 for the widest rows) in row groups
+// of TPR and one producer warp.  Tiles are RT = NC/TPR consecutive data rows.  A
 // stage holds the tile's data rows and, after them, only the distinct bias
 // rows those data rows use (at most `bias_slots`):
 //   inner broadcast: bias rows r0/ir .. (r0+nr-1)/ir, one contiguous copy;
@@ -209,8 +209,6 @@ __global__ void __launch_bounds__(256) k_bias_softmax_packed(const SmKernelArgs 
 // ---------------------------------------------------------------------------
 
 constexpr int kWsConsumers = 256;
-constexpr int kWsThreads = kWsConsumers + 32;
-constexpr int kWsConsumerWarps = kWsConsumers / 32;
 constexpr int kTmaMaxStages = 8;
 
 // EXACT: the row is exactly TPR*NV fragments, so no column needs a bounds check.
@@ -219,11 +217,12 @@ constexpr int kTmaMaxStages = 8;
 // (columns [p C/PARTS, (p+1) C/PARTS)) and the same part of its bias row, so
 // that stages stay small and two CTAs fit on an SM.  A lane's fragments
 // v in [p NV/PARTS, (p+1) NV/PARTS) lie in part p.
-template <typename T, int TPR, int NV, bool EXACT, int PARTS = 1>
-__global__ void __launch_bounds__(kWsThreads, EP_SM_TMA_MIN_CTAS)
+template <typename T, int TPR, int NV, bool EXACT, int PARTS = 1, int NC = kWsConsumers>
+__global__ void __launch_bounds__(NC + 32, NC > kWsConsumers ? 1 : EP_SM_TMA_MIN_CTAS)
 k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_t ntiles) {
   constexpr int VW = dev::Vec16<T>::N;
-  constexpr int RT = kWsConsumers / TPR;
+  constexpr int RT = NC / TPR;
+  constexpr int NCW = NC / 32;  // consumer warps
   static_assert(PARTS == 1 || (RT == 1 && EXACT && NV % PARTS == 0), "parts: one exact row a tile");
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[kTmaMaxStages];
@@ -232,8 +231,8 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
   __shared__ __align__(16) uint4 clc_resp;
   __shared__ int64_t tile_of[kTmaMaxStages];  // stage header: the tile, or -1
   __shared__ int slot_of[kTmaMaxStages][RT];  // sized per shape: static shared memory counts toward occupancy
-  __shared__ float red_a[kWsConsumerWarps];
-  __shared__ float red_b[kWsConsumerWarps];
+  __shared__ float red_a[NCW];
+  __shared__ float red_b[NCW];
 
   const int C = static_cast<int>(a.cols);  // staged rows are at most 64 KB
   // a stage holds rows, or one part of a row (and the same part of bias)
@@ -245,7 +244,7 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
   if (tid == 0) {
     for (int st = 0; st < stages; ++st) {
       dev::mbar_init(&full[st], 1);
-      dev::mbar_init(&empty[st], kWsConsumerWarps);
+      dev::mbar_init(&empty[st], NCW);
     }
     dev::mbar_init(&clc_bar, 1);
     dev::mbar_init_fence();
@@ -255,9 +254,9 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
   dev::pdl_trigger();
   if (int64_t(blockIdx.x) >= ntiles) return;
 
-  if (tid >= kWsConsumers) {
+  if (tid >= NC) {
     // ---- producer ----
-    if (tid != kWsConsumers) return;
+    if (tid != NC) return;
     const T* data = static_cast<const T*>(a.data);
     const T* bias = static_cast<const T*>(a.bias);
     const uint64_t pol_stream = dev::policy_evict_first();
@@ -1009,13 +1008,60 @@ inline int exact_tpr(int64_t nfrag, int nv) {
   return (t >= 4 && t <= 256 && (t & (t - 1)) == 0) ? static_cast<int>(t) : 0;
 }
 
+// Rows of 16385-32768 columns that 512 threads cover exactly (16-bit rows of
+// 20480, 24576, 28672 and 32768; float32 rows of every multiple of 2048): one
+// row a tile on 512 consumer threads holding NV fragments each (40-64
+// floats), staged with its bias row in NV/2 parts of 16 KB (NV odd: NV parts of
+// 8 KB); the CTA runs alone on its SM and takes as many stages as fit.
+constexpr int kWideTpr = 512;
+template <typename T, int NV>
+TmaRowFn wide_row_kernel() {
+  return k_bias_softmax_rows_tma<T, kWideTpr, NV, true, (NV % 2 == 0 ? NV / 2 : NV), kWideTpr>;
+}
+
 template <typename T>
-TmaRowFn pick_tma_row_kernel(int64_t cols, int* rows_per_tile, int* parts) {
+TmaRowFn pick_wide_row_kernel(int64_t nfrag, int* parts) {
+  constexpr int VW = dev::Vec16<T>::N;
+  if (nfrag % kWideTpr != 0) return nullptr;
+  const int64_t nv = nfrag / kWideTpr;
+  *parts = static_cast<int>(nv % 2 == 0 ? nv / 2 : nv);
+  if constexpr (VW == 8) {
+    switch (nv) {
+      case 5: return wide_row_kernel<T, 5>();
+      case 6: return wide_row_kernel<T, 6>();
+      case 7: return wide_row_kernel<T, 7>();
+      case 8: return wide_row_kernel<T, 8>();
+      default: return nullptr;
+    }
+  } else {
+    switch (nv) {
+      case 9: return wide_row_kernel<T, 9>();
+      case 10: return wide_row_kernel<T, 10>();
+      case 11: return wide_row_kernel<T, 11>();
+      case 12: return wide_row_kernel<T, 12>();
+      case 13: return wide_row_kernel<T, 13>();
+      case 14: return wide_row_kernel<T, 14>();
+      case 15: return wide_row_kernel<T, 15>();
+      case 16: return wide_row_kernel<T, 16>();
+      default: return nullptr;
+    }
+  }
+}
+
+template <typename T>
+TmaRowFn pick_tma_row_kernel(int64_t cols, int* rows_per_tile, int* parts, int* consumers) {
   *parts = 1;
+  *consumers = kWsConsumers;
   constexpr int VW = dev::Vec16<T>::N;
   const int64_t nfrag = cols / VW;
   const int64_t row_bytes = cols * int64_t(sizeof(T));
   if (nfrag < 12) return nullptr;
+  if (cols > kRowMax) {
+    if (!EP_SM_WIDE) return nullptr;
+    *rows_per_tile = 1;
+    *consumers = kWideTpr;
+    return pick_wide_row_kernel<T>(nfrag, parts);
+  }
   // exact shapes; the compiled set is every (TPR, NV) this search can return
   for (int nv : {4, 5, 6, 7, 8, 3, 12, 16}) {
     const int tpr = exact_tpr(nfrag, nv);
@@ -1076,7 +1122,8 @@ bool launch_tma_rows(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_count, 
                      int* launches, cudaError_t* err) {
   int rt = 0;
   int parts = 1;
-  TmaRowFn f = pick_tma_row_kernel<T>(a.cols, &rt, &parts);
+  int consumers = kWsConsumers;
+  TmaRowFn f = pick_tma_row_kernel<T>(a.cols, &rt, &parts, &consumers);
   if (f == nullptr) return false;
   // a stage holds a tile (or one part of a row) and its bias rows
   const uint32_t row_bytes = uint32_t(a.cols * int64_t(sizeof(T))) / uint32_t(parts);
@@ -1085,16 +1132,20 @@ bool launch_tma_rows(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_count, 
                                 : std::min<int64_t>(rt, a.bias_rows);
   const uint32_t stage_bytes = uint32_t(rt + slots) * row_bytes;
   if (2 * stage_bytes > 2 * kTmaStageBudget) return false;
-  const int stages = std::min<int>(kTmaMaxStages, std::max<int>(parts > 1 ? 3 : 2, kTmaStageBudget / stage_bytes));
+  int stages = std::min<int>(kTmaMaxStages, std::max<int>(parts > 1 ? 3 : 2, kTmaStageBudget / stage_bytes));
+  // the 512-thread CTAs fill the register file and run alone on their SM:
+  // as many stages as fit
+  if (consumers > kWsConsumers) stages = std::min<int>(kTmaMaxStages, int((224u * 1024u) / stage_bytes));
   const size_t smem = size_t(stages) * stage_bytes;
+  const int threads = consumers + 32;
   int per_sm = 1;
-  *err = resident_ctas(reinterpret_cast<const void*>(f), kWsThreads, smem, &per_sm);
+  *err = resident_ctas(reinterpret_cast<const void*>(f), threads, smem, &per_sm);
   if (*err != cudaSuccess) return true;
   const int64_t ntiles = (a.rows + rt - 1) / rt;
   // one CTA per tile under launch control, else a persistent grid
   const bool clc = EP_SM_CLC && ntiles <= int64_t(INT32_MAX);
   const unsigned grid = static_cast<unsigned>(clc ? ntiles : std::min<int64_t>(ntiles, int64_t(sm_count) * per_sm));
-  *err = launch(f, dim3(grid), dim3(kWsThreads), smem, stream, k, stages, int(slots), ntiles);
+  *err = launch(f, dim3(grid), dim3(threads), smem, stream, k, stages, int(slots), ntiles);
   if (*err == cudaSuccess) *launches += 1;
   return true;
 }

@@ -59,6 +59,11 @@
 #ifndef EP_SM_CLC
 #define EP_SM_CLC 1
 #endif
+// 1: rows of 16385-32768 columns that 512 threads cover exactly take the
+// staged row kernel with 512 consumer threads (0: the split-row pair).
+#ifndef EP_SM_WIDE
+#define EP_SM_WIDE 1
+#endif
 #ifndef EP_SM_TMA_MIN_TPR
 #define EP_SM_TMA_MIN_TPR 4
 #endif
