@@ -356,3 +356,44 @@ def test_wide_rows_masked_and_in_place(lib, dtype, cols):
     lib.ep_bias_softmax(x, d["bias"].cuda(), axis=1, is_inner_broadcast=0, output=x)
     torch.cuda.synchronize()
     assert torch.equal(x.cpu()[live], out[live])
+
+
+# ---------------------------------------------------------------------------
+# short rows (2 to 11 fragments, the register kernel's row groups of 4 to 16
+# threads): many CTAs, every bias layout, aligned and misaligned
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("nfrag", [2, 3, 4, 5, 6, 7, 8, 9, 10, 11])
+def test_short_rows_every_bias_layout(lib, dtype, nfrag):
+    cols = nfrag * (4 if dtype == "f32" else 8)
+    rows = 256 * 5 + 37
+    for bias_rows, inner in ((3, 0), (rows, 0), (rows // 16 + 1, 1) if rows % (rows // 16 + 1) == 0 else (1, 1),
+                             (1, 0)):
+        if rows % bias_rows:
+            continue
+        d = synth.bias_softmax_inputs((rows, cols), (bias_rows, cols), dtype, data_std=3.0, seed=cols + bias_rows)
+        out = run(lib, d["data"], d["bias"], 1, inner)
+        check(d["data"], d["bias"], 1, inner, out)
+
+
+@pytest.mark.parametrize("dtype,cols,bias_rows,inner", [("f16", 64, 1317, 0), ("f16", 32, 3, 1), ("f32", 32, 1, 0),
+                                                        ("f32", 24, 1317, 1), ("bf16", 88, 1317, 1)])
+def test_short_rows_bias_map_and_misaligned(lib, dtype, cols, bias_rows, inner):
+    rows = 1317
+    d = synth.bias_softmax_inputs((rows, cols), (bias_rows, cols), dtype, data_std=3.0, seed=cols + 5)
+    out = run(lib, d["data"], d["bias"], 1, inner)
+    check(d["data"], d["bias"], 1, inner, out)
+    es = 4 if dtype == "f32" else 2
+    out2 = run(lib, d["data"], d["bias"], 1, inner, offsets={"data": es, "output": es})   # scalar fragments
+    check(d["data"], d["bias"], 1, inner, out2)
+    # one-hot bias rows: the output row is exactly one-hot at its bias row's column
+    n = min(cols, bias_rows)
+    data = torch.zeros(rows, cols, dtype=d["data"].dtype)
+    bias = torch.full((bias_rows, cols), synth.MASKED, dtype=d["data"].dtype)
+    bias[torch.arange(bias_rows), torch.arange(bias_rows) % cols] = 0.0
+    got = run(lib, data, bias, 1, inner)
+    br = oracle.bias_row_of(np.arange(rows), bias_rows, rows // bias_rows, inner)
+    want = torch.zeros(rows, cols, dtype=data.dtype)
+    want[torch.arange(rows), torch.from_numpy(br % cols)] = 1.0
+    assert torch.equal(got, want), n

@@ -278,8 +278,12 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
   const uint32_t stage_bytes = 2 * tile_bytes;
   const bool has_beta = a.beta != nullptr;
   const bool has_bias = a.bias != nullptr;
-  // part-staged rows read gamma/beta/bias through the read-only path instead
-  const uint32_t param_bytes = PARTS > 1 ? 0u : param_stride * (1u + has_beta + has_bias);
+  // part-staged rows read bias through the read-only path, and gamma/beta too
+  // unless they are 16-bit rows whose host gave gamma/beta room in shared
+  // memory (param_stride != 0)
+  constexpr bool kPartParams = PARTS > 1 && sizeof(T) == 2;
+  const uint32_t param_bytes = PARTS > 1 ? (kPartParams ? param_stride * (1u + has_beta) : 0u)
+                                         : param_stride * (1u + has_beta + has_bias);
   unsigned char* stage0 = smem + param_bytes;
   const int tid = threadIdx.x;
 
@@ -305,7 +309,14 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
     const uint64_t pol_stream = dev::policy_evict_first();
     const uint64_t pol_keep = dev::policy_evict_last();
     if constexpr (PARTS > 1) {
-      dev::mbar_arrive(&params_bar);
+      if (!kPartParams || param_stride == 0) {
+        dev::mbar_arrive(&params_bar);
+      } else {
+        const uint32_t full_row = static_cast<uint32_t>(H) * uint32_t(sizeof(T));
+        dev::mbar_arrive_expect_tx(&params_bar, (1u + has_beta) * full_row);
+        dev::bulk_g2s(smem, a.gamma, full_row, &params_bar, pol_keep);
+        if (has_beta) dev::bulk_g2s(smem + param_stride, a.beta, full_row, &params_bar, pol_keep);
+      }
     } else {
       dev::mbar_arrive_expect_tx(&params_bar, param_bytes / param_stride * row_bytes);
       dev::bulk_g2s(smem, a.gamma, row_bytes, &params_bar, pol_keep);
@@ -392,7 +403,7 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
   const T* p_bias = reinterpret_cast<const T*>(smem + param_stride * (1u + has_beta));
   // a parameter fragment: from shared memory, or for part-staged rows from global
   auto param = [&](const T* staged, const void* global, int c, float (&f)[VW]) {
-    if constexpr (PARTS > 1) {
+    if (PARTS > 1 && (!kPartParams || param_stride == 0 || global == a.bias)) {
       dev::Frag<T, VW> q;
       q.load_keep(static_cast<const T*>(global) + c);
 #pragma unroll
@@ -722,7 +733,18 @@ cudaError_t launch_t(const SlnArgs& a, int sm_count, cudaStream_t stream, int* l
       const uint32_t row_bytes = uint32_t(a.H * int64_t(sizeof(T)));
       const uint32_t stage_bytes = 2u * uint32_t(rt) * row_bytes / uint32_t(parts);
       const uint32_t param_stride = (row_bytes + 127u) / 128u * 128u;
-      const uint32_t param_bytes = parts > 1 ? 0u : param_stride * (1u + (a.beta != nullptr) + (a.bias != nullptr));
+      uint32_t param_bytes = parts > 1 ? 0u : param_stride * (1u + (a.beta != nullptr) + (a.bias != nullptr));
+      // 16-bit 512-thread rows: gamma and beta in shared memory (they fit
+      // beside three stages up to 32768 elements)
+      uint32_t pstride = param_stride;
+      if (parts > 1) {
+        const uint32_t gb = param_stride * (1u + (a.beta != nullptr));
+        if (EP_SLN_WIDE_PARAMS && sizeof(T) == 2 && consumers > kWsConsumers && gb + 3u * stage_bytes <= 224u * 1024u) {
+          param_bytes = gb;
+        } else {
+          pstride = 0;
+        }
+      }
       int stages = std::min<int>(kTmaMaxStages, std::max<int>(parts > 1 ? 3 : 2, kTmaStageBudget / stage_bytes));
       // A CTA whose parameters and two stages already exceed half of shared
       // memory, or whose threads fill the register file, runs alone on its SM:
@@ -734,7 +756,10 @@ cudaError_t launch_t(const SlnArgs& a, int sm_count, cudaStream_t stream, int* l
                           param_bytes + 2u * stage_bytes <= kSmemForStages);
       if (alone)
         stages = std::min<int>(kTmaMaxStages, std::max<int>(stages, int((kSmemForStages - param_bytes) / stage_bytes)));
-      if (2 * stage_bytes <= 2 * kTmaStageBudget && param_bytes <= 96u * 1024u) {
+      // never more stages than fit beside the parameters
+      if (param_bytes + uint32_t(stages) * stage_bytes > kSmemForStages)
+        stages = std::max<int>(2, int((kSmemForStages - std::min(param_bytes, kSmemForStages)) / stage_bytes));
+      if (2 * stage_bytes <= 2 * kTmaStageBudget && (param_bytes <= 96u * 1024u || consumers > kWsConsumers)) {
         const size_t smem = param_bytes + size_t(stages) * stage_bytes;
         const int threads = consumers + 32;
         int per_sm = 1;
@@ -744,7 +769,7 @@ cudaError_t launch_t(const SlnArgs& a, int sm_count, cudaStream_t stream, int* l
         // one CTA per tile under launch control, else a persistent grid
         const bool clc = EP_SLN_CLC && ntiles <= int64_t(INT32_MAX);
         const unsigned grid = static_cast<unsigned>(clc ? ntiles : std::min<int64_t>(ntiles, int64_t(sm_count) * per_sm));
-        e = launch(f, dim3(grid), dim3(threads), smem, stream, k, stages, ntiles, param_stride);
+        e = launch(f, dim3(grid), dim3(threads), smem, stream, k, stages, ntiles, pstride);
         if (e == cudaSuccess) *launches += 1;
         return e;
       }

@@ -35,6 +35,11 @@
 #ifndef EP_SLN_WIDE
 #define EP_SLN_WIDE 1
 #endif
+// 1: those rows in 16-bit types keep gamma/beta in shared memory when they fit
+// beside three stages.
+#ifndef EP_SLN_WIDE_PARAMS
+#define EP_SLN_WIDE_PARAMS 1
+#endif
 // 1: one CTA per tile, running CTAs take over the tiles of CTAs they cancel
 // (cluster launch control); 0: persistent grid, tiles round-robin.
 #ifndef EP_SLN_CLC
