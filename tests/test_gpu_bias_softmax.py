@@ -320,11 +320,14 @@ def test_packed_rows_bias_map_bit_exact(lib):
 
 
 # ---------------------------------------------------------------------------
-# rows of 16385-32768 columns that 512 threads cover exactly: the staged row
-# kernel with 512 consumer threads, the row and its bias row staged in parts
+# rows of 16385-32768 columns on the staged row kernel with more than 256
+# consumer threads, the row and its bias row staged in parts: 16-bit rows of
+# 18432-30720 (multiples of 2048) on nfrag/4 threads of 4 fragments, 16-bit
+# rows of 32768 and float32 rows of multiples of 2048 on 512 threads
 # ---------------------------------------------------------------------------
 
-_WIDE = [("f16", 20480), ("f16", 24576), ("f16", 28672), ("f16", 32768), ("bf16", 20480), ("bf16", 32768),
+_WIDE = [("f16", 18432), ("f16", 20480), ("f16", 22528), ("f16", 24576), ("f16", 26624), ("f16", 28672),
+         ("f16", 30720), ("f16", 32768), ("bf16", 20480), ("bf16", 24576), ("bf16", 30720), ("bf16", 32768),
          ("f32", 18432), ("f32", 20480), ("f32", 22528), ("f32", 24576), ("f32", 26624), ("f32", 28672),
          ("f32", 30720), ("f32", 32768)]
 
@@ -338,7 +341,7 @@ def test_wide_rows_staged(lib, dtype, cols):
         check(d["data"], d["bias"], 1, inner, out)
 
 
-@pytest.mark.parametrize("dtype,cols", [("f16", 32768), ("f32", 20480)])
+@pytest.mark.parametrize("dtype,cols", [("f16", 32768), ("f16", 20480), ("bf16", 28672), ("f32", 20480)])
 def test_wide_rows_masked_and_in_place(lib, dtype, cols):
     rows = 40
     d = synth.bias_softmax_inputs((rows, cols), (rows, cols), dtype, data_std=2.0, seed=cols + 1)

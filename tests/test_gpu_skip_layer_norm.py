@@ -360,13 +360,16 @@ def test_ex_default_matches_plain_entry_point(lib):
 
 
 # ---------------------------------------------------------------------------
-# rows of 16385-32768 elements that 512 threads cover exactly: the staged
-# kernel with 512 consumer threads, the row staged in parts; many rows so
-# that tiles are taken over by running CTAs and the stage ring wraps
+# rows of 16385-32768 elements on the staged kernel with more than 256
+# consumer threads, the row staged in parts (16-bit rows of 18432-30720, in
+# multiples of 2048, on H/32 threads of 4 fragments; 16-bit rows of 32768 and
+# float32 rows of multiples of 2048 on 512 threads); many rows so that tiles
+# are taken over by running CTAs and the stage ring wraps
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("dtype,H", [("f16", 20480), ("f16", 24576), ("f16", 28672), ("f16", 32768),
-                                     ("bf16", 20480), ("bf16", 32768),
+@pytest.mark.parametrize("dtype,H", [("f16", 18432), ("f16", 20480), ("f16", 22528), ("f16", 24576),
+                                     ("f16", 26624), ("f16", 28672), ("f16", 30720), ("f16", 32768),
+                                     ("bf16", 20480), ("bf16", 28672), ("bf16", 32768),
                                      ("f32", 18432), ("f32", 20480), ("f32", 22528), ("f32", 24576),
                                      ("f32", 26624), ("f32", 28672), ("f32", 30720), ("f32", 32768)])
 def test_wide_rows_staged(lib, dtype, H):
@@ -379,6 +382,7 @@ def test_wide_rows_staged(lib, dtype, H):
 @pytest.mark.parametrize("dtype,H,beta,bias,res,skip_rows", [
     ("f16", 32768, False, False, False, None), ("f32", 20480, True, False, False, 5),
     ("bf16", 24576, False, True, True, 7), ("f32", 32768, True, True, True, None),
+    ("f16", 20480, False, True, False, 7), ("bf16", 30720, True, False, True, None),
 ])
 def test_wide_rows_optional_inputs_and_broadcast_skip(lib, dtype, H, beta, bias, res, skip_rows):
     rows = 161

@@ -380,14 +380,11 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
         }
         const T* s_d = reinterpret_cast<const T*>(smem + size_t(ring.st) * stage_bytes);
         const T* s_b = reinterpret_cast<const T*>(smem + size_t(ring.st) * stage_bytes + data_bytes);
+        // one row a tile (RT == 1): the tile's row always exists
 #pragma unroll
         for (int v = p * PV; v < (p + 1) * PV; ++v) {
           const int c = (v * TPR + lane) * VW - p * part_cols;
-          float b[VW];
-          dev::lds_unpack(s_d + c, z[v]);
-          dev::lds_unpack(s_b + c, b);
-#pragma unroll
-          for (int e = 0; e < VW; ++e) z[v][e] = active ? z[v][e] + b[e] : -INFINITY;
+          dev::lds_add(s_d + c, s_b + c, z[v]);
         }
         __syncwarp();
         if ((tid & 31) == 0) dev::mbar_arrive(&empty[ring.st]);
@@ -400,11 +397,7 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
       for (int v = 0; v < NV; ++v) {
         const int c = (v * TPR + lane) * VW;
         if (active && (EXACT || c < C)) {
-          float b[VW];
-          dev::lds_unpack(s_d + c, z[v]);
-          dev::lds_unpack(s_b + c, b);
-#pragma unroll
-          for (int e = 0; e < VW; ++e) z[v][e] += b[e];
+          dev::lds_add(s_d + c, s_b + c, z[v]);
         } else {
 #pragma unroll
           for (int e = 0; e < VW; ++e) z[v][e] = -INFINITY;
@@ -418,18 +411,41 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
 #pragma unroll
     for (int v = 0; v < NV; ++v)
 #pragma unroll
-      for (int e = 0; e < VW; ++e) m = fmaxf(m, z[v][e]);
+      for (int e = 0; e < VW; e += 2) m = dev::max3(m, z[v][e], z[v][e + 1]);
     m = dev::group_max_named<TPR>(m, red_a, bar_id, gwarp0);
     float sum = 0.f;
+    if constexpr (sizeof(T) == 2 && EP_SM_LEAN16) {
+      // 16-bit results: the exponent z log2e - m log2e as one packed fused
+      // multiply-add per pair (its extra rounding, a few float32 ulp of
+      // |m log2e|, is far below a 16-bit result's spacing), and two sums
+      float2 acc = make_float2(0.f, 0.f);
+      const float2 l2 = make_float2(dev::kLog2e, dev::kLog2e);
+      const float2 ml = make_float2(-m * dev::kLog2e, -m * dev::kLog2e);
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      const int c = (v * TPR + lane) * VW;
+      for (int v = 0; v < NV; ++v) {
+        const int c = (v * TPR + lane) * VW;
 #pragma unroll
-      for (int e = 0; e < VW; ++e) {
-        float ev = dev::ex2_approx((z[v][e] - m) * dev::kLog2e);
-        if (!EXACT && c >= C) ev = 0.f;
-        z[v][e] = ev;
-        sum += ev;
+        for (int e = 0; e < VW; e += 2) {
+          const float2 t = __ffma2_rn(make_float2(z[v][e], z[v][e + 1]), l2, ml);
+          float e0 = dev::ex2_approx(t.x), e1 = dev::ex2_approx(t.y);
+          if (!EXACT && c >= C) e0 = e1 = 0.f;
+          z[v][e] = e0;
+          z[v][e + 1] = e1;
+          acc = __fadd2_rn(acc, make_float2(e0, e1));
+        }
+      }
+      sum = acc.x + acc.y;
+    } else {
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int c = (v * TPR + lane) * VW;
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          float ev = dev::ex2_approx((z[v][e] - m) * dev::kLog2e);
+          if (!EXACT && c >= C) ev = 0.f;
+          z[v][e] = ev;
+          sum += ev;
+        }
       }
     }
     sum = dev::group_sum_named<TPR>(sum, red_b, bar_id, gwarp0);
@@ -440,8 +456,7 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
       for (int v = 0; v < NV; ++v) {
         const int c = (v * TPR + lane) * VW;
         if (EXACT || c < C) {
-#pragma unroll
-          for (int e = 0; e < VW; ++e) z[v][e] *= inv;
+          dev::scale_pairs(z[v], inv);
           dev::stg_pack_stream(orow + c, z[v]);
         }
       }
@@ -1019,6 +1034,34 @@ TmaRowFn wide_row_kernel() {
   return k_bias_softmax_rows_tma<T, kWideTpr, NV, true, (NV % 2 == 0 ? NV / 2 : NV), kWideTpr>;
 }
 
+// 16-bit rows of 18432-30720 columns (multiples of 2048): 4 fragments a
+// thread on nfrag / 4 consumer threads (576-960, whole warps), the row staged
+// in halves.  Against 512 threads holding 5-7 fragments each, the extra warps
+// hide more of each row's reductions: 0.50-0.62 of the copy bandwidth became
+// 0.65-0.73 (rows of 24576 and 32768, which 512 threads cover with 6 and 8
+// fragments, measured the same either way; four parts a row measured slower).
+template <typename T, int TPR>
+TmaRowFn wide4_row_kernel() {
+  return k_bias_softmax_rows_tma<T, TPR, 4, true, 2, TPR>;
+}
+
+template <typename T>
+TmaRowFn pick_wide4_row_kernel(int64_t nfrag, int* parts, int* consumers) {
+  if (nfrag % 256 != 0) return nullptr;
+  *parts = 2;
+  *consumers = static_cast<int>(nfrag / 4);
+  switch (nfrag / 4) {
+    case 576: return wide4_row_kernel<T, 576>();
+    case 640: return wide4_row_kernel<T, 640>();
+    case 704: return wide4_row_kernel<T, 704>();
+    case 768: return wide4_row_kernel<T, 768>();
+    case 832: return wide4_row_kernel<T, 832>();
+    case 896: return wide4_row_kernel<T, 896>();
+    case 960: return wide4_row_kernel<T, 960>();
+    default: return nullptr;
+  }
+}
+
 template <typename T>
 TmaRowFn pick_wide_row_kernel(int64_t nfrag, int* parts) {
   constexpr int VW = dev::Vec16<T>::N;
@@ -1059,6 +1102,10 @@ TmaRowFn pick_tma_row_kernel(int64_t cols, int* rows_per_tile, int* parts, int* 
   if (cols > kRowMax) {
     if (!EP_SM_WIDE) return nullptr;
     *rows_per_tile = 1;
+    if constexpr (VW == 8) {
+      if (EP_SM_WIDE_NV4)
+        if (TmaRowFn f = pick_wide4_row_kernel<T>(nfrag, parts, consumers)) return f;
+    }
     *consumers = kWideTpr;
     return pick_wide_row_kernel<T>(nfrag, parts);
   }

@@ -120,6 +120,89 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction (NaN operands ignored, as fmaxf does).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// z = data + bias for one 16-byte fragment: the bias unpacked to float32, each
+// 16-bit data element added to it by one mixed-precision add (the exact
+// float32 value of the element plus the float32 bias, rounded once, as a
+// conversion followed by a float32 add).  float32 fragments add in pairs.
+template <typename T> struct MixAdd;
+template <> struct MixAdd<__half> {
+  static __device__ __forceinline__ void add(uint32_t w, float b0, float b1, float& z0, float& z1) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.f16 %0, l, %3;\n\tadd.rn.f32.f16 %1, h, %4;\n\t}"
+        : "=&f"(z0), "=f"(z1) : "r"(w), "f"(b0), "f"(b1));
+  }
+};
+template <> struct MixAdd<__nv_bfloat16> {
+  static __device__ __forceinline__ void add(uint32_t w, float b0, float b1, float& z0, float& z1) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %3;\n\tadd.rn.f32.bf16 %1, h, %4;\n\t}"
+        : "=&f"(z0), "=f"(z1) : "r"(w), "f"(b0), "f"(b1));
+  }
+};
+
+// z += b for a raw 16-byte fragment b of T (16-bit: one mixed-precision add
+// per element; float32: packed adds), each sum rounded once to float32.
+template <typename T, int VW>
+__device__ __forceinline__ void add_raw(uint4 b, float (&z)[VW]);
+
+// Element-wise z += b and z *= k over a fragment, two lanes per packed
+// float32 instruction (each lane rounded exactly as the scalar operation).
+template <int VW>
+__device__ __forceinline__ void add_pairs(float (&z)[VW], const float (&b)[VW]) {
+#pragma unroll
+  for (int e = 0; e < VW; e += 2) {
+    const float2 t = __fadd2_rn(make_float2(z[e], z[e + 1]), make_float2(b[e], b[e + 1]));
+    z[e] = t.x;
+    z[e + 1] = t.y;
+  }
+}
+template <int VW>
+__device__ __forceinline__ void scale_pairs(float (&z)[VW], float k) {
+#pragma unroll
+  for (int e = 0; e < VW; e += 2) {
+    const float2 t = __fmul2_rn(make_float2(z[e], z[e + 1]), make_float2(k, k));
+    z[e] = t.x;
+    z[e + 1] = t.y;
+  }
+}
+
+template <typename T, int VW>
+__device__ __forceinline__ void add_raw(uint4 b, float (&z)[VW]) {
+  if constexpr (sizeof(T) == 2) {
+    const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) MixAdd<T>::add(w[i], z[2 * i], z[2 * i + 1], z[2 * i], z[2 * i + 1]);
+  } else {
+    float fb[VW];
+    Conv<T>::unpack(b, fb);
+    add_pairs(z, fb);
+  }
+}
+
+template <typename T, int VW>
+__device__ __forceinline__ void lds_add(const T* d, const T* b, float (&z)[VW]) {
+  if constexpr (sizeof(T) == 2) {
+    float fb[VW];
+    Conv<T>::unpack(*reinterpret_cast<const uint4*>(b), fb);
+    const uint4 u = *reinterpret_cast<const uint4*>(d);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) MixAdd<T>::add(w[i], fb[2 * i], fb[2 * i + 1], z[2 * i], z[2 * i + 1]);
+  } else {
+    float fb[VW];
+    Conv<T>::unpack(*reinterpret_cast<const uint4*>(d), z);
+    Conv<T>::unpack(*reinterpret_cast<const uint4*>(b), fb);
+    add_pairs(z, fb);
+  }
+}
+
 // 16-byte shared-memory load of T elements, unpacked to float32; and a
 // 16-byte evict-first global store of float32 lanes packed to T.
 template <typename T, int VW>
@@ -173,10 +256,18 @@ __device__ __forceinline__ float group_sum(float x, float* red) {
     if ((threadIdx.x & 31) == 0) red[warp] = x;
     __syncthreads();
     const float* g = red + (warp / W) * W;
-    float t = 0.f;
+    if constexpr (W > 8) {
+      const int l = threadIdx.x & 31;
+      float t = l < W ? g[l] : 0.f;
 #pragma unroll
-    for (int i = 0; i < W; ++i) t += g[i];
-    return t;
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      return t;
+    } else {
+      float t = 0.f;
+#pragma unroll
+      for (int i = 0; i < W; ++i) t += g[i];
+      return t;
+    }
   }
 }
 
@@ -194,10 +285,18 @@ __device__ __forceinline__ float group_max(float x, float* red) {
     if ((threadIdx.x & 31) == 0) red[warp] = x;
     __syncthreads();
     const float* g = red + (warp / W) * W;
-    float t = g[0];
+    if constexpr (W > 8) {
+      const int l = threadIdx.x & 31;
+      float t = l < W ? g[l] : -INFINITY;
 #pragma unroll
-    for (int i = 1; i < W; ++i) t = fmaxf(t, g[i]);
-    return t;
+      for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
+      return t;
+    } else {
+      float t = g[0];
+#pragma unroll
+      for (int i = 1; i < W; ++i) t = fmaxf(t, g[i]);
+      return t;
+    }
   }
 }
 
@@ -205,6 +304,9 @@ __device__ __forceinline__ float group_max(float x, float* red) {
 // shuffles within the warp segment; TPR > 32 (whole warps) uses a named
 // barrier `bar_id` over the group's TPR threads and the group's slots of
 // `red` (indexed by warp within the group: `gwarp0` is the group's first warp).
+// Groups of more than 8 warps combine the warps' slots lane-parallel (lane i
+// reads slot i, then a butterfly over the warp), which takes fewer
+// instructions than every thread adding all the slots in turn.
 template <int TPR>
 __device__ __forceinline__ float group_sum_named(float x, float* red, int bar_id, int gwarp0) {
   if constexpr (TPR <= 32) {
@@ -218,10 +320,18 @@ __device__ __forceinline__ float group_sum_named(float x, float* red, int bar_id
     const int warp = threadIdx.x >> 5;
     if ((threadIdx.x & 31) == 0) red[warp] = x;
     asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(TPR) : "memory");
-    float t = 0.f;
+    if constexpr (W > 8) {
+      const int l = threadIdx.x & 31;
+      float t = l < W ? red[gwarp0 + l] : 0.f;
 #pragma unroll
-    for (int i = 0; i < W; ++i) t += red[gwarp0 + i];
-    return t;
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      return t;
+    } else {
+      float t = 0.f;
+#pragma unroll
+      for (int i = 0; i < W; ++i) t += red[gwarp0 + i];
+      return t;
+    }
   }
 }
 
@@ -238,10 +348,18 @@ __device__ __forceinline__ float group_max_named(float x, float* red, int bar_id
     const int warp = threadIdx.x >> 5;
     if ((threadIdx.x & 31) == 0) red[warp] = x;
     asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(TPR) : "memory");
-    float t = red[gwarp0];
+    if constexpr (W > 8) {
+      const int l = threadIdx.x & 31;
+      float t = l < W ? red[gwarp0 + l] : -INFINITY;
 #pragma unroll
-    for (int i = 1; i < W; ++i) t = fmaxf(t, red[gwarp0 + i]);
-    return t;
+      for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
+      return t;
+    } else {
+      float t = red[gwarp0];
+#pragma unroll
+      for (int i = 1; i < W; ++i) t = fmaxf(t, red[gwarp0 + i]);
+      return t;
+    }
   }
 }
 

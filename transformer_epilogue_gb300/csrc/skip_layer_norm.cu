@@ -412,6 +412,28 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
       dev::lds_unpack(staged + c, f);
     }
   };
+  // the same fragment as 16 raw bytes
+  auto param_raw = [&](const T* staged, const void* global, int c) -> uint4 {
+    if (PARTS > 1 && (!kPartParams || param_stride == 0 || global == a.bias))
+      return dev::ld16_keep(static_cast<const T*>(global) + c);
+    return dev::lds16(staged + c);
+  };
+  // 16-bit types: mixed-precision adds and packed float32 pairs take fewer
+  // instructions (16-bit rows of 12288-32768 elements went from 0.78-0.90 of
+  // the copy bandwidth to 0.93-0.97); float32 rows, which hold up to 64 values
+  // a thread, keep scalar arithmetic, which needs fewer registers
+  constexpr bool kLean = sizeof(T) == 2;
+  auto load_sum = [&](const T* in, const T* sk, float (&f)[VW]) {
+    if constexpr (kLean) {
+      dev::lds_add(in, sk, f);
+    } else {
+      float k[VW];
+      dev::lds_unpack(in, f);
+      dev::lds_unpack(sk, k);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) f[e] = __fadd_rn(f[e], k[e]);
+    }
+  };
   const int g = tid / TPR;
   const int lane = tid % TPR;
   const int bar_id = 1 + g;            // named barrier of a multi-warp group
@@ -444,14 +466,11 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
         const unsigned char* stage = stage0 + size_t(ring.st) * stage_bytes;
         const T* s_in = reinterpret_cast<const T*>(stage);
         const T* s_sk = reinterpret_cast<const T*>(stage + tile_bytes);
+        // one row a tile (RT == 1): the tile's row always exists
 #pragma unroll
         for (int v = p * PV; v < (p + 1) * PV; ++v) {
           const int c = (v * TPR + lane) * VW - p * part_cols;
-          float k[VW];
-          dev::lds_unpack(s_in + c, s[v]);
-          dev::lds_unpack(s_sk + c, k);
-#pragma unroll
-          for (int e = 0; e < VW; ++e) s[v][e] = active ? __fadd_rn(s[v][e], k[e]) : 0.f;
+          load_sum(s_in + c, s_sk + c, s[v]);
         }
         __syncwarp();
         if ((tid & 31) == 0) dev::mbar_arrive(&empty[ring.st]);
@@ -464,11 +483,7 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
       for (int v = 0; v < NV; ++v) {
         const int c = (v * TPR + lane) * VW;
         if (active && (EXACT || c < H)) {
-          float k[VW];
-          dev::lds_unpack(s_in + c, s[v]);
-          dev::lds_unpack(s_sk + c, k);
-#pragma unroll
-          for (int e = 0; e < VW; ++e) s[v][e] = __fadd_rn(s[v][e], k[e]);
+          load_sum(s_in + c, s_sk + c, s[v]);
         } else {
 #pragma unroll
           for (int e = 0; e < VW; ++e) s[v][e] = 0.f;
@@ -485,36 +500,68 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
         const int c = (v * TPR + lane) * VW;
         if (EXACT || c < H) {
           if (has_bias) {
-            float b[VW];
-            param(p_bias, a.bias, c, b);
+            if constexpr (kLean) {
+              dev::add_raw<T>(param_raw(p_bias, a.bias, c), s[v]);
+            } else {
+              float b[VW];
+              param(p_bias, a.bias, c, b);
 #pragma unroll
-            for (int e = 0; e < VW; ++e) s[v][e] = __fadd_rn(s[v][e], b[e]);
+              for (int e = 0; e < VW; ++e) s[v][e] = __fadd_rn(s[v][e], b[e]);
+            }
           }
           if (sum_out != nullptr) dev::stg_pack_stream(sum_out + off + c, s[v]);
         }
       }
     }
     float mean = 0.f;
-    if (!a.simplified) {
-      float t = 0.f;
+    float var;
+    if constexpr (kLean) {
+      // sums over pairs of lanes (packed float32), then the two halves
+      if (!a.simplified) {
+        float2 t2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int v = 0; v < NV; ++v)
+        for (int v = 0; v < NV; ++v)
 #pragma unroll
-        for (int e = 0; e < VW; ++e) t += s[v][e];
-      mean = dev::group_sum_named<TPR>(t, red_a, bar_id, gwarp0) / static_cast<float>(H);
-    }
-    // s becomes s - mean from here on
-    float q = 0.f;
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      const int c = (v * TPR + lane) * VW;
-#pragma unroll
-      for (int e = 0; e < VW; ++e) {
-        s[v][e] -= mean;
-        if (EXACT || c < H) q = fmaf(s[v][e], s[v][e], q);
+          for (int e = 0; e < VW; e += 2) t2 = __fadd2_rn(t2, make_float2(s[v][e], s[v][e + 1]));
+        mean = dev::group_sum_named<TPR>(t2.x + t2.y, red_a, bar_id, gwarp0) / static_cast<float>(H);
       }
+      // s becomes s - mean from here on
+      float2 q2 = make_float2(0.f, 0.f);
+      const float2 nm = make_float2(-mean, -mean);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int c = (v * TPR + lane) * VW;
+#pragma unroll
+        for (int e = 0; e < VW; e += 2) {
+          const float2 d = __fadd2_rn(make_float2(s[v][e], s[v][e + 1]), nm);
+          s[v][e] = d.x;
+          s[v][e + 1] = d.y;
+          if (EXACT || c < H) q2 = __ffma2_rn(d, d, q2);
+        }
+      }
+      var = dev::group_sum_named<TPR>(q2.x + q2.y, red_b, bar_id, gwarp0) / static_cast<float>(H);
+    } else {
+      if (!a.simplified) {
+        float t = 0.f;
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+#pragma unroll
+          for (int e = 0; e < VW; ++e) t += s[v][e];
+        mean = dev::group_sum_named<TPR>(t, red_a, bar_id, gwarp0) / static_cast<float>(H);
+      }
+      // s becomes s - mean from here on
+      float q = 0.f;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int c = (v * TPR + lane) * VW;
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          s[v][e] -= mean;
+          if (EXACT || c < H) q = fmaf(s[v][e], s[v][e], q);
+        }
+      }
+      var = dev::group_sum_named<TPR>(q, red_b, bar_id, gwarp0) / static_cast<float>(H);
     }
-    const float var = dev::group_sum_named<TPR>(q, red_b, bar_id, gwarp0) / static_cast<float>(H);
     const float rstd = 1.0f / sqrtf(var + a.eps);
     if (active) {
       if (lane == 0) {
@@ -527,14 +574,35 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
         if (EXACT || c < H) {
           float gm[VW], y[VW];
           param(p_gamma, a.gamma, c, gm);
-          if (has_beta) {
+          const float2 rs = make_float2(rstd, rstd);
+          if constexpr (!kLean) {
+            if (has_beta) {
+              float bt[VW];
+              param(p_beta, a.beta, c, bt);
+#pragma unroll
+              for (int e = 0; e < VW; ++e) y[e] = fmaf(s[v][e] * rstd, gm[e], bt[e]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < VW; ++e) y[e] = (s[v][e] * rstd) * gm[e];
+            }
+          } else if (has_beta) {
             float bt[VW];
             param(p_beta, a.beta, c, bt);
 #pragma unroll
-            for (int e = 0; e < VW; ++e) y[e] = fmaf(s[v][e] * rstd, gm[e], bt[e]);
+            for (int e = 0; e < VW; e += 2) {
+              const float2 t = __ffma2_rn(__fmul2_rn(make_float2(s[v][e], s[v][e + 1]), rs),
+                                          make_float2(gm[e], gm[e + 1]), make_float2(bt[e], bt[e + 1]));
+              y[e] = t.x;
+              y[e + 1] = t.y;
+            }
           } else {
 #pragma unroll
-            for (int e = 0; e < VW; ++e) y[e] = (s[v][e] * rstd) * gm[e];
+            for (int e = 0; e < VW; e += 2) {
+              const float2 t = __fmul2_rn(__fmul2_rn(make_float2(s[v][e], s[v][e + 1]), rs),
+                                          make_float2(gm[e], gm[e + 1]));
+              y[e] = t.x;
+              y[e + 1] = t.y;
+            }
           }
           dev::stg_pack_stream(out + off + c, y);
         }
@@ -622,6 +690,35 @@ TmaFn wide_kernel() {
   return k_skip_layer_norm_tma<T, kWideTpr, NV, true, (NV % 2 == 0 ? NV / 2 : NV), kWideTpr>;
 }
 
+// 16-bit rows of 18432-30720 elements (multiples of 2048 other than 24576): 4
+// fragments a thread on nfrag / 4 consumer threads (576-960, whole warps); more warps than
+// 512 threads holding 5-7 fragments hide more of each row's two reductions.
+// The row is staged in halves, or in quarters above 24576 elements, so that
+// gamma and beta still fit in shared memory beside three stages.  (Rows of
+// 24576 stay on 512 threads of 6 fragments: 0.91 of the copy bandwidth
+// against 0.88 on 768 threads of 4; 28672 went from 0.82 to 0.91 on 896.)
+template <int TPR> constexpr int wide4_parts() { return TPR > 768 ? 4 : 2; }
+template <typename T, int TPR>
+TmaFn wide4_kernel() {
+  return k_skip_layer_norm_tma<T, TPR, 4, true, wide4_parts<TPR>(), TPR>;
+}
+
+template <typename T>
+TmaFn pick_wide4_kernel(int64_t nfrag, int* parts, int* consumers) {
+  if (nfrag % 256 != 0) return nullptr;
+  *parts = nfrag / 4 > 768 ? wide4_parts<832>() : wide4_parts<576>();
+  *consumers = static_cast<int>(nfrag / 4);
+  switch (nfrag / 4) {
+    case 576: return wide4_kernel<T, 576>();
+    case 640: return wide4_kernel<T, 640>();
+    case 704: return wide4_kernel<T, 704>();
+    case 832: return wide4_kernel<T, 832>();
+    case 896: return wide4_kernel<T, 896>();
+    case 960: return wide4_kernel<T, 960>();
+    default: return nullptr;
+  }
+}
+
 template <typename T>
 TmaFn pick_wide_kernel(int64_t nfrag, int* parts) {
   constexpr int VW = dev::Vec16<T>::N;
@@ -660,6 +757,10 @@ TmaFn pick_tma_kernel(int64_t H, int* rows_per_tile, int* parts, int* consumers)
   if (nfrag < 4) return nullptr;
   if (EP_SLN_WIDE && H > 16384) {
     *rows_per_tile = 1;
+    if constexpr (VW == 8) {
+      if (EP_SLN_WIDE_NV4)
+        if (TmaFn f = pick_wide4_kernel<T>(nfrag, parts, consumers)) return f;
+    }
     *consumers = kWideTpr;
     return pick_wide_kernel<T>(nfrag, parts);
   }

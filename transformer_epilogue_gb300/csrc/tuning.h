@@ -40,6 +40,12 @@
 #ifndef EP_SLN_WIDE_PARAMS
 #define EP_SLN_WIDE_PARAMS 1
 #endif
+// 1: 16-bit rows of 18432-30720 elements (multiples of 2048 other than 24576)
+// take 4 fragments a thread on H/32 consumer threads (0: 512 threads where
+// they cover the row).
+#ifndef EP_SLN_WIDE_NV4
+#define EP_SLN_WIDE_NV4 1
+#endif
 // 1: one CTA per tile, running CTAs take over the tiles of CTAs they cancel
 // (cluster launch control); 0: persistent grid, tiles round-robin.
 #ifndef EP_SLN_CLC
@@ -68,6 +74,16 @@
 // staged row kernel with 512 consumer threads (0: the split-row pair).
 #ifndef EP_SM_WIDE
 #define EP_SM_WIDE 1
+#endif
+// 1: 16-bit rows of 18432-30720 columns (multiples of 2048) take 4 fragments
+// a thread on nfrag/4 consumer threads (0: 512 threads where they cover the row).
+#ifndef EP_SM_WIDE_NV4
+#define EP_SM_WIDE_NV4 1
+#endif
+// 1: staged softmax rows of 16-bit types form the exponent with one packed
+// fused multiply-add per pair of elements.
+#ifndef EP_SM_LEAN16
+#define EP_SM_LEAN16 1
 #endif
 #ifndef EP_SM_TMA_MIN_TPR
 #define EP_SM_TMA_MIN_TPR 4
