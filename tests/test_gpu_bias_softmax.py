@@ -294,14 +294,18 @@ def test_split_ranges_cross_rows_with_masked_chunks(lib, dtype, cols):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
-@pytest.mark.parametrize("cols", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("cols", [1, 2, 3, 4, 5, 8])
 @pytest.mark.parametrize("inner", [0, 1])
-def test_packed_rows(lib, dtype, cols, inner):
-    # rows of <= 8 elements: one thread per row
+@pytest.mark.parametrize("misaligned", [False, True])
+def test_packed_rows(lib, dtype, cols, inner, misaligned):
+    # rows of <= 8 elements: one thread per row (aligned rows of exactly 8
+    # elements: the register kernel's one-thread rows; a data pointer one
+    # element off sends them to the packed kernel)
     rows = 70007 if inner else 70000
     bias_rows = 7 if inner else 16
     d = synth.bias_softmax_inputs((rows, cols), (bias_rows, cols), dtype, data_std=3.0, seed=cols)
-    out = run(lib, d["data"], d["bias"], 1, inner)
+    offs = {"data": d["data"].element_size()} if misaligned else None
+    out = run(lib, d["data"], d["bias"], 1, inner, offsets=offs)
     sample = sorted(set(synth.sample_rows(rows, 3000)) | set(range(rows - 5, rows)))
     check(d["data"], d["bias"], 1, inner, out, rows=sample)
 

@@ -57,13 +57,16 @@ __device__ __forceinline__ int64_t bias_row(const SmKernelArgs& a, int64_t r) {
   return a.inner ? r / a.inner_repeat : r % a.bias_rows;
 }
 
-template <typename T, int VW, int TPR, int NV>
+template <typename T, int VW, int TPR, int NV, bool EXACT = false>
 __global__ void __launch_bounds__(TPR > 256 ? TPR : 256)
 k_bias_softmax_rows(const SmKernelArgs a) {
   dev::pdl_wait();
   dev::pdl_trigger();
   constexpr int BS = TPR > 256 ? TPR : 256;
   constexpr int RPC = BS / TPR;
+  // 16-byte fragments of a 16-bit type: data added to the bias by
+  // mixed-precision adds, the exponent as a packed fused multiply-add
+  constexpr bool k16 = sizeof(T) == 2 && VW == 8;
   __shared__ float red_a[BS / 32];
   __shared__ float red_b[BS / 32];
   const T* data = static_cast<const T*>(a.data);  // may alias output (in place)
@@ -76,59 +79,113 @@ k_bias_softmax_rows(const SmKernelArgs a) {
   for (int64_t base = int64_t(blockIdx.x) * RPC; base < a.rows; base += int64_t(gridDim.x) * RPC) {
     const int64_t r = base + g;
     const bool active = r < a.rows;
-    Frag<T, VW> z[NV];
+    const int64_t off = r * C;
+    float z[NV][VW];
 #pragma unroll
     for (int v = 0; v < NV; ++v)
 #pragma unroll
-      for (int e = 0; e < VW; ++e) z[v].v[e] = -INFINITY;
+      for (int e = 0; e < VW; ++e) z[v][e] = -INFINITY;
     if (active) {
-      const int64_t off = r * C;
       const int64_t boff = bias_row(a, r) * C;
-      Frag<T, VW> b[NV];
+      if constexpr (k16) {
+        // all loads first (raw 16-byte fragments), then one fragment at a time
+        uint4 du[NV], bu[NV];
 #pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        const int64_t c = int64_t(v * TPR + lane) * VW;
-        if (c < C) {
-          z[v].load_stream(data + off + c);
-          b[v].load_keep(bias + boff + c);
+        for (int v = 0; v < NV; ++v) {
+          const int c = (v * TPR + lane) * VW;
+          if (EXACT || c < C) {
+            du[v] = dev::ld16_stream(data + off + c);
+            bu[v] = dev::ld16_keep(bias + boff + c);
+          }
         }
-      }
 #pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        const int64_t c = int64_t(v * TPR + lane) * VW;
-        if (c < C) {
+        for (int v = 0; v < NV; ++v) {
+          const int c = (v * TPR + lane) * VW;
+          if (EXACT || c < C) {
+            float bz[VW];
+            dev::Conv<T>::unpack(bu[v], bz);
+            const uint32_t w[4] = {du[v].x, du[v].y, du[v].z, du[v].w};
 #pragma unroll
-          for (int e = 0; e < VW; ++e) z[v].v[e] = z[v].v[e] + b[v].v[e];
+            for (int i = 0; i < 4; ++i)
+              dev::MixAdd<T>::add(w[i], bz[2 * i], bz[2 * i + 1], z[v][2 * i], z[v][2 * i + 1]);
+          }
+        }
+      } else {
+        Frag<T, VW> d[NV], b[NV];
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+          const int64_t c = int64_t(v * TPR + lane) * VW;
+          if (EXACT || c < C) {
+            d[v].load_stream(data + off + c);
+            b[v].load_keep(bias + boff + c);
+          }
+        }
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+          const int64_t c = int64_t(v * TPR + lane) * VW;
+          if (EXACT || c < C) {
+#pragma unroll
+            for (int e = 0; e < VW; ++e) z[v][e] = d[v].v[e] + b[v].v[e];
+          }
         }
       }
     }
     float m = -INFINITY;
 #pragma unroll
-    for (int v = 0; v < NV; ++v)
+    for (int v = 0; v < NV; ++v) {
+      if constexpr (VW % 2 == 0) {
 #pragma unroll
-      for (int e = 0; e < VW; ++e) m = fmaxf(m, z[v].v[e]);
+        for (int e = 0; e < VW; e += 2) m = dev::max3(m, z[v][e], z[v][e + 1]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) m = fmaxf(m, z[v][e]);
+      }
+    }
     m = dev::group_max<TPR>(m, red_a);
     float s = 0.f;
+    if constexpr (k16) {
+      float2 acc = make_float2(0.f, 0.f);
+      const float2 l2 = make_float2(dev::kLog2e, dev::kLog2e);
+      const float2 ml = make_float2(-m * dev::kLog2e, -m * dev::kLog2e);
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      const int64_t c = int64_t(v * TPR + lane) * VW;
+      for (int v = 0; v < NV; ++v) {
+        const int c = (v * TPR + lane) * VW;
 #pragma unroll
-      for (int e = 0; e < VW; ++e) {
-        z[v].v[e] = (c < C) ? __expf(z[v].v[e] - m) : 0.f;
-        s += z[v].v[e];
+        for (int e = 0; e < VW; e += 2) {
+          const float2 t = __ffma2_rn(make_float2(z[v][e], z[v][e + 1]), l2, ml);
+          float e0 = dev::ex2_approx(t.x), e1 = dev::ex2_approx(t.y);
+          if (!EXACT && c >= C) e0 = e1 = 0.f;
+          z[v][e] = e0;
+          z[v][e + 1] = e1;
+          acc = __fadd2_rn(acc, make_float2(e0, e1));
+        }
+      }
+      s = acc.x + acc.y;
+    } else {
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int64_t c = int64_t(v * TPR + lane) * VW;
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          z[v][e] = (EXACT || c < C) ? __expf(z[v][e] - m) : 0.f;
+          s += z[v][e];
+        }
       }
     }
     s = dev::group_sum<TPR>(s, red_b);
     const float inv = 1.0f / s;
     if (active) {
-      const int64_t off = r * C;
 #pragma unroll
       for (int v = 0; v < NV; ++v) {
         const int64_t c = int64_t(v * TPR + lane) * VW;
-        if (c < C) {
+        if (EXACT || c < C) {
+          if constexpr (VW % 2 == 0) dev::scale_pairs(z[v], inv);
+          else {
 #pragma unroll
-          for (int e = 0; e < VW; ++e) z[v].v[e] *= inv;
-          z[v].store_stream(out + off + c);
+            for (int e = 0; e < VW; ++e) z[v][e] *= inv;
+          }
+          if constexpr (VW == 1) dev::st1_stream(out + off + c, z[v][0]);
+          else dev::stg_pack_stream(out + off + c, z[v]);
         }
       }
     }
@@ -913,6 +970,26 @@ RowFn pick_row_kernel(int64_t cols, int* tpr_out) {
     *tpr_out = TPR_;                                 \
     return k_bias_softmax_rows<T, VW, TPR_, NV_>;    \
   }
+  // Rows of 2-11 16-byte fragments: groups of 1-4 threads holding 2-3
+  // fragments each, exact where a power-of-two group covers the row (no column
+  // checks).  Against groups of 4, 8 or 16 threads holding one fragment this
+  // amortises each row's reductions and reciprocal over more elements: float16
+  // rows of 32 and 64 columns went from 0.58 to 0.84-0.86 of the copy
+  // bandwidth, float32 rows of 16 and 32 from 0.77 to 0.99.
+#define EP_SM_SHORT_X(N_, TPR_, NV_, EX_) \
+  case N_: *tpr_out = TPR_; return k_bias_softmax_rows<T, VW, TPR_, NV_, EX_>;
+  if constexpr (VW > 1) {
+    if (nfrag * VW == cols && nfrag >= 1 && nfrag <= 11) {
+      switch (nfrag) {
+        EP_SM_SHORT_X(1, 1, 1, true) EP_SM_SHORT_X(2, 1, 2, true) EP_SM_SHORT_X(3, 1, 3, true) EP_SM_SHORT_X(4, 2, 2, true)
+        EP_SM_SHORT_X(5, 1, 5, true) EP_SM_SHORT_X(6, 2, 3, true) EP_SM_SHORT_X(7, 1, 7, true)
+        EP_SM_SHORT_X(8, 4, 2, true) EP_SM_SHORT_X(9, 1, 9, true) EP_SM_SHORT_X(10, 2, 5, true)
+        EP_SM_SHORT_X(11, 1, 11, true)
+        default: break;
+      }
+    }
+  }
+#undef EP_SM_SHORT_X
   if constexpr (VW == 8) {
     EP_SM_CASE(4, 1) EP_SM_CASE(8, 1) EP_SM_CASE(16, 1)
     EP_SM_CASE(32, 1) EP_SM_CASE(32, 2) EP_SM_CASE(32, 4) EP_SM_CASE(64, 4)
@@ -1202,7 +1279,11 @@ cudaError_t launch_t(const SoftmaxArgs& a, int sm_count, int l2_bytes, cudaStrea
   constexpr int VW = dev::Vec16<T>::N;
   SmKernelArgs k{a.data, a.bias, a.output, a.rows, a.cols, a.bias_rows, a.inner_repeat, a.inner};
   const bool vec = vec_ok<T>(a.data, a.bias, a.output, a.cols);
-  if (a.cols <= kPackedMax) {
+  // aligned rows of exactly 8 elements (one 16-bit fragment, or two float32
+  // ones) take the register kernel's one-thread rows: 0.23 -> 0.74 (float16)
+  // and 0.34 -> 0.99 (float32) of the copy bandwidth; float32 rows of 4 stay
+  // here (0.69 against 0.59)
+  if (a.cols <= kPackedMax && !(vec && EP_SM_SHORT_VEC && a.cols == kPackedMax)) {
     const int64_t blocks = (a.rows + 255) / 256;
     const unsigned grid = static_cast<unsigned>(std::min<int64_t>(blocks, int64_t(sm_count) * 32));
     cudaError_t el = launch(k_bias_softmax_packed<T>, dim3(grid), dim3(256), 0, stream, k);

@@ -85,6 +85,11 @@
 #ifndef EP_SM_LEAN16
 #define EP_SM_LEAN16 1
 #endif
+// 1: 16-byte-aligned rows of exactly 8 elements take the register kernel's
+// one-thread rows; 0: the packed kernel.
+#ifndef EP_SM_SHORT_VEC
+#define EP_SM_SHORT_VEC 1
+#endif
 #ifndef EP_SM_TMA_MIN_TPR
 #define EP_SM_TMA_MIN_TPR 4
 #endif
