@@ -698,11 +698,7 @@ __device__ __forceinline__ void split_load_z(const T* sd, const T* sb, int c0, i
   for (int v = 0; v < NV; ++v) {
     const int c = c0 + v * 32 * VW;
     if (WHOLE || c < tw) {
-      float b[VW];
-      dev::lds_unpack(sd + c, z[v]);
-      dev::lds_unpack(sb + c, b);
-#pragma unroll
-      for (int e = 0; e < VW; ++e) z[v][e] += b[e];
+      dev::lds_add(sd + c, sb + c, z[v]);
     } else {
 #pragma unroll
       for (int e = 0; e < VW; ++e) z[v][e] = -INFINITY;
@@ -718,8 +714,21 @@ __device__ __forceinline__ void split_store_y(T* orow, int c0, int tw, const flo
     const int c = c0 + v * 32 * VW;
     if (WHOLE || c < tw) {
       float y[VW];
+      if constexpr (sizeof(T) == 2) {
+        // 16-bit results: the exponent as one packed fused multiply-add per pair
+        const float2 l2 = make_float2(dev::kLog2e, dev::kLog2e);
+        const float2 ml = make_float2(-h.x * dev::kLog2e, -h.x * dev::kLog2e);
 #pragma unroll
-      for (int e = 0; e < VW; ++e) y[e] = dev::ex2_approx((z[v][e] - h.x) * dev::kLog2e) * h.y;
+        for (int e = 0; e < VW; e += 2) {
+          const float2 t = __ffma2_rn(make_float2(z[v][e], z[v][e + 1]), l2, ml);
+          y[e] = dev::ex2_approx(t.x);
+          y[e + 1] = dev::ex2_approx(t.y);
+        }
+        dev::scale_pairs(y, h.y);
+      } else {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) y[e] = dev::ex2_approx((z[v][e] - h.x) * dev::kLog2e) * h.y;
+      }
       dev::stg_pack_stream(orow + c, y);
     }
   }
@@ -891,18 +900,34 @@ k_softmax_split_tma(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t n
 #pragma unroll
         for (int v = 0; v < NV; ++v)
 #pragma unroll
-          for (int e = 0; e < VW; ++e) cm = fmaxf(cm, z[v][e]);
+          for (int e = 0; e < VW; e += 2) cm = dev::max3(cm, z[v][e], z[v][e + 1]);
         const float mn = fmaxf(ml, cm);
         if (mn != -INFINITY) {
           float acc0 = sl * dev::ex2_approx((ml - mn) * dev::kLog2e);  // ml = -inf gives 0
           float acc1 = 0.f;
+          if constexpr (sizeof(T) == 2) {
+            // 16-bit data: the exponent as one packed fused multiply-add per pair
+            const float2 l2 = make_float2(dev::kLog2e, dev::kLog2e);
+            const float2 nl = make_float2(-mn * dev::kLog2e, -mn * dev::kLog2e);
+            float2 acc = make_float2(acc0, acc1);
 #pragma unroll
-          for (int v = 0; v < NV; ++v)
+            for (int v = 0; v < NV; ++v)
 #pragma unroll
-            for (int e = 0; e < VW; e += 2) {
-              acc0 += dev::ex2_approx((z[v][e] - mn) * dev::kLog2e);
-              acc1 += dev::ex2_approx((z[v][e + 1] - mn) * dev::kLog2e);
-            }
+              for (int e = 0; e < VW; e += 2) {
+                const float2 t = __ffma2_rn(make_float2(z[v][e], z[v][e + 1]), l2, nl);
+                acc = __fadd2_rn(acc, make_float2(dev::ex2_approx(t.x), dev::ex2_approx(t.y)));
+              }
+            acc0 = acc.x;
+            acc1 = acc.y;
+          } else {
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+#pragma unroll
+              for (int e = 0; e < VW; e += 2) {
+                acc0 += dev::ex2_approx((z[v][e] - mn) * dev::kLog2e);
+                acc1 += dev::ex2_approx((z[v][e + 1] - mn) * dev::kLog2e);
+              }
+          }
           sl = acc0 + acc1;
           ml = mn;
         }
