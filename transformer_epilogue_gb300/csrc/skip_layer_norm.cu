@@ -697,21 +697,35 @@ TmaFn wide_kernel() {
 // gamma and beta still fit in shared memory beside three stages.  (Rows of
 // 24576 stay on 512 threads of 6 fragments: 0.91 of the copy bandwidth
 // against 0.88 on 768 threads of 4; 28672 went from 0.82 to 0.91 on 896.)
-template <int TPR> constexpr int wide4_parts() { return TPR > 768 ? 4 : 2; }
+// float32 rows of 26624-30720 take 8 fragments (32 floats) a thread on the
+// same H/32 threads, staged in quarters: 0.73-0.85 of the copy bandwidth on
+// 512 threads of 13-15 fragments (which spill), 0.88-0.90 here; shorter float32
+// rows measured 3-4 % slower this way and stay on 512 threads.
+template <typename T, int TPR> constexpr int wide4_parts() {
+  return sizeof(T) == 4 ? 4 : (TPR > 768 ? 4 : 2);
+}
 template <typename T, int TPR>
 TmaFn wide4_kernel() {
-  return k_skip_layer_norm_tma<T, TPR, 4, true, wide4_parts<TPR>(), TPR>;
+  constexpr int NV = 32 / dev::Vec16<T>::N;  // 32 elements a thread
+  return k_skip_layer_norm_tma<T, TPR, NV, true, wide4_parts<T, TPR>(), TPR>;
 }
 
 template <typename T>
 TmaFn pick_wide4_kernel(int64_t nfrag, int* parts, int* consumers) {
-  if (nfrag % 256 != 0) return nullptr;
-  *parts = nfrag / 4 > 768 ? wide4_parts<832>() : wide4_parts<576>();
-  *consumers = static_cast<int>(nfrag / 4);
-  switch (nfrag / 4) {
-    case 576: return wide4_kernel<T, 576>();
-    case 640: return wide4_kernel<T, 640>();
-    case 704: return wide4_kernel<T, 704>();
+  constexpr int NV = 32 / dev::Vec16<T>::N;
+  if (nfrag % (64 * NV) != 0) return nullptr;
+  const int64_t tpr = nfrag / NV;
+  *parts = tpr > 768 ? wide4_parts<T, 832>() : wide4_parts<T, 576>();
+  *consumers = static_cast<int>(tpr);
+  if constexpr (sizeof(T) == 2) {
+    switch (tpr) {
+      case 576: return wide4_kernel<T, 576>();
+      case 640: return wide4_kernel<T, 640>();
+      case 704: return wide4_kernel<T, 704>();
+      default: break;
+    }
+  }
+  switch (tpr) {
     case 832: return wide4_kernel<T, 832>();
     case 896: return wide4_kernel<T, 896>();
     case 960: return wide4_kernel<T, 960>();
@@ -757,10 +771,8 @@ TmaFn pick_tma_kernel(int64_t H, int* rows_per_tile, int* parts, int* consumers)
   if (nfrag < 4) return nullptr;
   if (EP_SLN_WIDE && H > 16384) {
     *rows_per_tile = 1;
-    if constexpr (VW == 8) {
-      if (EP_SLN_WIDE_NV4)
-        if (TmaFn f = pick_wide4_kernel<T>(nfrag, parts, consumers)) return f;
-    }
+    if (VW == 8 ? EP_SLN_WIDE_NV4 : EP_SLN_WIDE_NV8)
+      if (TmaFn f = pick_wide4_kernel<T>(nfrag, parts, consumers)) return f;
     *consumers = kWideTpr;
     return pick_wide_kernel<T>(nfrag, parts);
   }

@@ -46,6 +46,10 @@
 #ifndef EP_SLN_WIDE_NV4
 #define EP_SLN_WIDE_NV4 1
 #endif
+// 1: float32 rows of those lengths take 8 fragments a thread on H/32 threads.
+#ifndef EP_SLN_WIDE_NV8
+#define EP_SLN_WIDE_NV8 1
+#endif
 // 1: one CTA per tile, running CTAs take over the tiles of CTAs they cancel
 // (cluster launch control); 0: persistent grid, tiles round-robin.
 #ifndef EP_SLN_CLC
