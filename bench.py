@@ -78,16 +78,16 @@ ORDER = [
 # step serves from L2), and writes still dirty in L2 when a kernel ends are not
 # counted.
 NCU_TRAFFIC = {
-    "bias_add_f16_16x1024x4096": 348818176,
-    "bias_softmax_f16_32x16x512x512_causal": 492905728,
-    "bias_softmax_f32_64x262144_cyclic": 153313280,
-    "bias_softmax_f32_8x1048576": 75636224,
-    "quick_gelu_f16_67108867": 207132160,
-    "sln_f16_16384x4096_bias_residual": 476495616,
-    "sln_f32_2x128x768": 1608704,
-    "sln_f32_32x2048x1024_bcast_skip": 486595072,
+    "bias_add_f16_16x1024x4096": 356219904,
+    "bias_softmax_f16_32x16x512x512_causal": 495425280,
+    "bias_softmax_f32_64x262144_cyclic": 153383936,
+    "bias_softmax_f32_8x1048576": 75631360,
+    "quick_gelu_f16_67108867": 210809088,
+    "sln_f16_16384x4096_bias_residual": 479364352,
+    "sln_f32_2x128x768": 1608960,
+    "sln_f32_32x2048x1024_bcast_skip": 488912384,
 }
-NCU_TRAFFIC_SOURCE_HASH = "d27bdb1b7430f42d"
+NCU_TRAFFIC_SOURCE_HASH = "7590974382f3ceab"
 
 
 def kernel_source_hash() -> str:
@@ -419,6 +419,36 @@ def run_profile(args):
     return 0
 
 
+def run_profile_shape(args):
+    """Runs one shape outside the bench workloads `--reps` times and nothing
+    else (a target for ncu): softmax:DTYPE:ROWS:COLS (8 cyclic bias rows) or
+    sln:DTYPE:ROWS:H (beta, bias and the residual output)."""
+    import transformer_epilogue_gb300 as te
+    te.load_library()
+    op, dts, rows, cols = args.profile_shape.split(":")
+    rows, cols = int(rows), int(cols)
+    dt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[dts]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    x = torch.randn(rows, cols, device="cuda", generator=g).to(dt)
+    o = torch.empty_like(x)
+    if op == "softmax":
+        b = torch.randn(8, cols, device="cuda", generator=g).to(dt)
+        fn = lambda: te.ep_bias_softmax(x, b, axis=1, is_inner_broadcast=0, output=o)
+    elif op == "sln":
+        sk = torch.randn(rows, cols, device="cuda", generator=g).to(dt)
+        r = torch.empty_like(x)
+        gm, bt, bi = (torch.randn(cols, device="cuda", generator=g).to(dt) for _ in range(3))
+        fn = lambda: te.ep_skip_layer_norm(x, sk, gm, bt, bi, 1e-12, output=o, input_skip_bias_sum=r)
+    else:
+        raise ValueError(f"unknown op {op!r} (softmax or sln)")
+    for _ in range(args.reps):
+        fn()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_shape": args.profile_shape, "reps": args.reps}), flush=True)
+    return 0
+
+
 def run_reference(args, ws, rank):
     """The reference arm: the float64 CPU oracle, as it stands, on bounded
     samples of the same workloads (rank 0 only)."""
@@ -465,10 +495,13 @@ def main(argv=None):
     ap.add_argument("--profile", choices=ORDER, help="run only this workload --reps times (for ncu)")
     ap.add_argument("--batch", type=int, default=0, help="with --profile: cut the leading dimension to this")
     ap.add_argument("--reps", type=int, default=3, help="with --profile: calls of the op")
+    ap.add_argument("--profile-shape", help="softmax|sln:DTYPE:ROWS:COLS: run that shape --reps times (for ncu)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     if args.profile:
         return run_profile(args)
+    if args.profile_shape:
+        return run_profile_shape(args)
 
     ws, rank, local = dist_env()
     if ws > 1:
