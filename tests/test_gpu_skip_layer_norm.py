@@ -80,13 +80,37 @@ def test_manifest_combinations(lib, combo, H):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f16"])
-@pytest.mark.parametrize("H", [1, 2, 3, 4, 5, 7, 8, 9, 31, 32, 33, 64, 127, 128, 129, 255, 256, 257, 500, 511, 512,
+@pytest.mark.parametrize("H", [1, 2, 3, 4, 5, 7, 8, 9, 12, 16, 24, 31, 32, 33, 64, 127, 128, 129, 255, 256, 257, 500, 511, 512,
                                513, 1000, 1023, 1024, 1025, 2048, 2049, 4096, 4100, 8192, 8200, 12288, 16384])
 def test_hidden_sizes(lib, dtype, H):
     rows = 19 if H <= 4096 else 5
     d = synth.sln_inputs((rows, H), None, dtype, has_beta=True, has_bias=True, seed=H)
     out, s = run(lib, d, residual=True)
     check(d, out, s)
+
+
+@pytest.mark.parametrize("dtype,H", [("f32", 8), ("f32", 12), ("f16", 16), ("f16", 24), ("bf16", 16), ("bf16", 24)])
+@pytest.mark.parametrize("skip_rows", [None, 7])
+@pytest.mark.parametrize("simplified", [False, True])
+def test_short_rows_one_thread(lib, dtype, H, skip_rows, simplified):
+    # aligned rows of 2 or 3 fragments: one thread a row on the register kernel
+    # (256 rows a CTA), with a broadcast skip, the residual output and the
+    # statistics outputs
+    rows = 256 * 5 + 37 if skip_rows is None else 7 * 187
+    if skip_rows is None:
+        d = synth.sln_inputs((rows, H), None, dtype, has_beta=not simplified, has_bias=True, seed=H + 9)
+    else:
+        d = synth.sln_inputs((rows // skip_rows, skip_rows, H), (1, skip_rows, H), dtype, has_beta=not simplified,
+                             has_bias=True, seed=H + 9)
+    out, s, mean, inv = run_ex(lib, d, simplified)
+    o = oracle.skip_layer_norm(d["input"], d["skip"], d["gamma"], d["beta"], d["bias"], d["epsilon"],
+                               simplified=simplified)
+    assert_norm_close(out.reshape(-1, H), o["output"].reshape(-1, H), d["input"].dtype)
+    assert_bit_exact(s.reshape(-1, H), oracle.skip_bias_sum(d["input"], d["skip"], d["bias"]).reshape(-1, H))
+    np.testing.assert_allclose(mean.numpy().astype(np.float64).reshape(-1), o["mean"].reshape(-1), rtol=2e-5,
+                               atol=2e-6)
+    np.testing.assert_allclose(inv.numpy().astype(np.float64).reshape(-1), o["inv_std_dev"].reshape(-1), rtol=2e-5,
+                               atol=0)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f16"])

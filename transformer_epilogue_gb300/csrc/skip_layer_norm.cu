@@ -840,6 +840,19 @@ cudaError_t launch_t(const SlnArgs& a, int sm_count, cudaStream_t stream, int* l
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   const bool vec = (a.H % VW == 0) && al16(a.input) && al16(a.skip) && al16(a.gamma) &&
                    al16(a.beta) && al16(a.bias) && al16(a.output) && al16(a.sum_out);
+  // rows of 2 or 3 fragments: one thread a row on the register kernel, which
+  // runs no reduction across threads (256 MB: float32 H = 8 and 12 0.56-0.74 ->
+  // 0.98-1.00 of the copy bandwidth, float16 H = 16 0.41 -> 0.69; rows of 4
+  // fragments measured slower this way than on 4-thread staged rows)
+  if (vec && EP_SLN_SHORT_REG && a.H / VW >= 2 && a.H / VW <= 3) {
+    KernelFn fn = a.H / VW == 2 ? k_skip_layer_norm<T, VW, 1, 2> : k_skip_layer_norm<T, VW, 1, 3>;
+    const int64_t need = (a.rows + 255) / 256;
+    const int64_t cap = int64_t(sm_count) * 64 * 8;
+    cudaError_t el = launch(fn, dim3(static_cast<unsigned>(std::min(need, cap))), dim3(256), 0, stream, k);
+    if (el != cudaSuccess) return el;
+    *launches += 1;
+    return cudaGetLastError();
+  }
   if (vec && EP_SLN_TMA) {
     int rt = 0, parts = 1, consumers = kWsConsumers;
     if (TmaFn f = pick_tma_kernel<T>(a.H, &rt, &parts, &consumers)) {

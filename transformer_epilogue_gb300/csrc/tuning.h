@@ -50,6 +50,10 @@
 #ifndef EP_SLN_WIDE_NV8
 #define EP_SLN_WIDE_NV8 1
 #endif
+// 1: aligned rows of 2 or 3 fragments take one thread a row on the register kernel.
+#ifndef EP_SLN_SHORT_REG
+#define EP_SLN_SHORT_REG 1
+#endif
 // 1: one CTA per tile, running CTAs take over the tiles of CTAs they cancel
 // (cluster launch control); 0: persistent grid, tiles round-robin.
 #ifndef EP_SLN_CLC
