@@ -11,8 +11,10 @@
 // Row path (rows of at most 16384 elements): a group of TPR threads owns a row;
 // z is kept in float32 registers, so data and output cross HBM once.  Max and
 // sum are warp-shuffle (+ named-barrier) reductions.  16-byte-aligned rows take
-// the staged kernel (k_bias_softmax_rows_tma), others the register kernel;
-// rows of at most 8 elements a thread-per-row kernel.
+// the staged kernel (k_bias_softmax_rows_tma) from 12 fragments on and the
+// register kernel below that; other rows the register kernel; rows of at most
+// 8 elements that are not one or two whole aligned fragments a thread-per-row
+// kernel.
 //
 // Split-row path (longer rows): rows are cut into 16 KB chunks and a pair of
 // launches runs over them:
@@ -995,12 +997,14 @@ RowFn pick_row_kernel(int64_t cols, int* tpr_out) {
     *tpr_out = TPR_;                                 \
     return k_bias_softmax_rows<T, VW, TPR_, NV_>;    \
   }
-  // Rows of 2-11 16-byte fragments: groups of 1-4 threads holding 2-3
-  // fragments each, exact where a power-of-two group covers the row (no column
-  // checks).  Against groups of 4, 8 or 16 threads holding one fragment this
-  // amortises each row's reductions and reciprocal over more elements: float16
-  // rows of 32 and 64 columns went from 0.58 to 0.84-0.86 of the copy
-  // bandwidth, float32 rows of 16 and 32 from 0.77 to 0.99.
+  // Rows of 1-11 16-byte fragments: groups of 1, 2 or 4 threads holding 1-11
+  // fragments each, every shape exact (no column checks).  Against groups of
+  // 4, 8 or 16 threads holding one fragment this shares each row's reductions,
+  // reciprocal and index arithmetic among more elements a thread: at 256 MB
+  // float16 rows of 32 and 64 columns went from 0.58 to 0.98-0.99 of the copy
+  // bandwidth, float32 rows of 16 and 32 from 0.77 to 1.0; a thread holding a
+  // whole row of 7, 9 or 11 fragments reaches 0.61-0.78 (groups of 4 threads
+  // with idle lanes measured slower).
 #define EP_SM_SHORT_X(N_, TPR_, NV_, EX_) \
   case N_: *tpr_out = TPR_; return k_bias_softmax_rows<T, VW, TPR_, NV_, EX_>;
   if constexpr (VW > 1) {
@@ -1015,12 +1019,13 @@ RowFn pick_row_kernel(int64_t cols, int* tpr_out) {
     }
   }
 #undef EP_SM_SHORT_X
+  // (16-byte fragments: rows of up to 11 fragments never get here)
   if constexpr (VW == 8) {
-    EP_SM_CASE(4, 1) EP_SM_CASE(8, 1) EP_SM_CASE(16, 1)
+    EP_SM_CASE(16, 1)
     EP_SM_CASE(32, 1) EP_SM_CASE(32, 2) EP_SM_CASE(32, 4) EP_SM_CASE(64, 4)
     EP_SM_CASE(128, 4) EP_SM_CASE(256, 4) EP_SM_CASE(512, 4)
   } else if constexpr (VW == 4) {
-    EP_SM_CASE(4, 1) EP_SM_CASE(8, 1) EP_SM_CASE(16, 1)
+    EP_SM_CASE(16, 1)
     EP_SM_CASE(32, 1) EP_SM_CASE(32, 2) EP_SM_CASE(32, 4) EP_SM_CASE(32, 8)
     EP_SM_CASE(64, 8) EP_SM_CASE(128, 8) EP_SM_CASE(256, 8) EP_SM_CASE(512, 8)
   } else {
