@@ -13,8 +13,7 @@
 // sum are warp-shuffle (+ named-barrier) reductions.  16-byte-aligned rows take
 // the staged kernel (k_bias_softmax_rows_tma) from 12 fragments on and the
 // register kernel below that; other rows the register kernel; rows of at most
-// 8 elements that are not one or two whole aligned fragments a thread-per-row
-// kernel.
+// 8 elements, other than aligned rows of exactly 8, a thread-per-row kernel.
 //
 // Split-row path (longer rows): rows are cut into 16 KB chunks and a pair of
 // launches runs over them:
