@@ -444,8 +444,7 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
           const int c = (v * TPR + lane) * VW - p * part_cols;
           dev::lds_add(s_d + c, s_b + c, z[v]);
         }
-        __syncwarp();
-        if ((tid & 31) == 0) dev::mbar_arrive(&empty[ring.st]);
+        dev::release_stage(&empty[ring.st]);
       }
     } else {
       const unsigned char* stage = smem + size_t(st) * stage_bytes;
@@ -461,8 +460,7 @@ k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_
           for (int e = 0; e < VW; ++e) z[v][e] = -INFINITY;
         }
       }
-      __syncwarp();
-      if ((tid & 31) == 0) dev::mbar_arrive(&empty[st]);
+      dev::release_stage(&empty[st]);
     }
 
     float m = z[0][0];
@@ -893,8 +891,7 @@ k_softmax_split_tma(const SmKernelArgs a, int64_t row0, int64_t nrows, int64_t n
       else split_load_z<T, NV, VW, false>(sd, sb, c0, tw, z);
       float2 h = make_float2(0.f, 0.f);
       if (!STATS) h = hdr[st];
-      __syncwarp();
-      if (lane == 0) dev::mbar_arrive(&empty[st]);
+      dev::release_stage(&empty[st]);
 
       if constexpr (STATS) {
         float cm = -INFINITY;
@@ -997,23 +994,36 @@ RowFn pick_row_kernel(int64_t cols, int* tpr_out) {
     return k_bias_softmax_rows<T, VW, TPR_, NV_>;    \
   }
   // Rows of 1-11 16-byte fragments: groups of 1, 2 or 4 threads holding 1-11
-  // fragments each, every shape exact (no column checks).  Against groups of
-  // 4, 8 or 16 threads holding one fragment this shares each row's reductions,
-  // reciprocal and index arithmetic among more elements a thread: at 256 MB
-  // float16 rows of 32 and 64 columns went from 0.58 to 0.98-0.99 of the copy
-  // bandwidth, float32 rows of 16 and 32 from 0.77 to 1.0; a thread holding a
-  // whole row of 7, 9 or 11 fragments reaches 0.61-0.78 (groups of 4 threads
-  // with idle lanes measured slower).
+  // fragments each, exact (no column checks) but for float32 rows of 7, 9 and
+  // 11 fragments.  Against groups of 4, 8 or 16 threads holding one fragment
+  // this shares each row's reductions, reciprocal and index arithmetic among
+  // more elements a thread: at 256 MB float16 rows of 32 and 64 columns went
+  // from 0.58 to 0.98-0.99 of the copy bandwidth, float32 rows of 16 and 32
+  // from 0.77 to 1.0 (groups of 4 threads with idle lanes measured slower).
 #define EP_SM_SHORT_X(N_, TPR_, NV_, EX_) \
   case N_: *tpr_out = TPR_; return k_bias_softmax_rows<T, VW, TPR_, NV_, EX_>;
   if constexpr (VW > 1) {
     if (nfrag * VW == cols && nfrag >= 1 && nfrag <= 11) {
       switch (nfrag) {
         EP_SM_SHORT_X(1, 1, 1, true) EP_SM_SHORT_X(2, 1, 2, true) EP_SM_SHORT_X(3, 1, 3, true) EP_SM_SHORT_X(4, 2, 2, true)
-        EP_SM_SHORT_X(5, 1, 5, true) EP_SM_SHORT_X(6, 2, 3, true) EP_SM_SHORT_X(7, 1, 7, true)
-        EP_SM_SHORT_X(8, 4, 2, true) EP_SM_SHORT_X(9, 1, 9, true) EP_SM_SHORT_X(10, 2, 5, true)
-        EP_SM_SHORT_X(11, 1, 11, true)
+        EP_SM_SHORT_X(5, 1, 5, true) EP_SM_SHORT_X(6, 2, 3, true)
+        EP_SM_SHORT_X(8, 4, 2, true) EP_SM_SHORT_X(10, 2, 5, true)
         default: break;
+      }
+      // 7, 9 or 11 fragments: a thread holding the whole row (16-bit, 0.71-0.77
+      // of the copy bandwidth against 0.59-0.67 on two threads with an idle
+      // fragment); float32 rows, whose one-thread form holds 28-44 floats, run
+      // better on two threads (0.74 / 0.64 / 0.69 against 0.71 / 0.61 / 0.62)
+      if constexpr (VW == 4) {
+        switch (nfrag) {
+          EP_SM_SHORT_X(7, 2, 4, false) EP_SM_SHORT_X(9, 2, 5, false) EP_SM_SHORT_X(11, 2, 6, false)
+          default: break;
+        }
+      } else {
+        switch (nfrag) {
+          EP_SM_SHORT_X(7, 1, 7, true) EP_SM_SHORT_X(9, 1, 9, true) EP_SM_SHORT_X(11, 1, 11, true)
+          default: break;
+        }
       }
     }
   }

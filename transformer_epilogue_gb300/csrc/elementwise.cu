@@ -381,8 +381,7 @@ k_elementwise_tma(const T* x, const T* skip, const T* bias, T* y, int64_t nfrag,
         if constexpr (BIAS_ADD) dev::lds_unpack(reinterpret_cast<const T*>(src + kTileBytes) + f * VW, sk[u]);
       }
     }
-    __syncwarp();
-    if ((tid & 31) == 0) dev::mbar_arrive(&empty[st]);
+    dev::release_stage(&empty[st]);
     uint32_t c = 0;
     if constexpr (BIAS_ADD) {
       c = col0 + uint32_t(tid) * VW;

@@ -472,8 +472,7 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
           const int c = (v * TPR + lane) * VW - p * part_cols;
           load_sum(s_in + c, s_sk + c, s[v]);
         }
-        __syncwarp();
-        if ((tid & 31) == 0) dev::mbar_arrive(&empty[ring.st]);
+        dev::release_stage(&empty[ring.st]);
       }
     } else {
       const unsigned char* stage = stage0 + size_t(st) * stage_bytes;
@@ -489,8 +488,7 @@ k_skip_layer_norm_tma(const SlnKernelArgs a, int stages, int64_t ntiles, uint32_
           for (int e = 0; e < VW; ++e) s[v][e] = 0.f;
         }
       }
-      __syncwarp();
-      if ((tid & 31) == 0) dev::mbar_arrive(&empty[st]);
+      dev::release_stage(&empty[st]);
     }
 
     const int64_t off = r * H;

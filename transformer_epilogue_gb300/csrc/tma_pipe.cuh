@@ -109,6 +109,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
       : "memory");
 }
 
+// A consumer warp hands a stage back to the producer.  The warp's reads of
+// the stage go through the generic proxy, the producer's next bulk copy into
+// it through the async proxy: a proxy fence orders every lane's reads before
+// that copy (without it a copy into a stage whose last reads were still
+// queued measured as stale data in the stage's final fragments), then lane 0
+// arrives on `empty`.
+__device__ __forceinline__ void release_stage(uint64_t* empty_bar) {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(empty_bar);
+}
+
 // Named barrier over `count` threads (a multiple of 32) with id 1..15; returns
 // true on every participating thread iff `pred` held on all of them.
 __device__ __forceinline__ bool named_barrier_and(int id, int count, bool pred) {
