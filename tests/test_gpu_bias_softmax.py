@@ -345,6 +345,18 @@ def test_wide_rows_staged(lib, dtype, cols):
         check(d["data"], d["bias"], 1, inner, out)
 
 
+@pytest.mark.parametrize("dtype,cols", [("f32", 32768), ("f16", 20480)])
+def test_wide_rows_stage_reuse_repeated(lib, dtype, cols):
+    # stages refilled as soon as the consumers hand them back (see the
+    # SkipLayerNorm test of the same name): eight calls must all match
+    rows, bias_rows = 258, 3
+    d = synth.bias_softmax_inputs((rows, cols), (bias_rows, cols), dtype, data_std=2.0, seed=cols + 3)
+    o = oracle.bias_softmax(d["data"], d["bias"], axis=1, is_inner_broadcast=0)
+    for _ in range(8):
+        out = run(lib, d["data"], d["bias"], 1, 0)
+        assert_norm_close(out.reshape(rows, cols), o, d["data"].dtype)
+
+
 @pytest.mark.parametrize("dtype,cols", [("f16", 32768), ("f16", 20480), ("bf16", 28672), ("f32", 20480)])
 def test_wide_rows_masked_and_in_place(lib, dtype, cols):
     rows = 40

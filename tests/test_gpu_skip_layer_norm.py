@@ -403,6 +403,22 @@ def test_wide_rows_staged(lib, dtype, H):
     check(d, out, s)
 
 
+def test_wide_rows_stage_reuse_repeated(lib):
+    # float32 rows of 28672: one row fills the four 56 KB stages, so every
+    # stage is refilled with the next row's part as soon as the consumers hand
+    # it back.  Without a proxy fence between the consumers' reads and that
+    # refill, about one call in five had a row whose last fragment held the
+    # next row's data; eight calls must all match the oracle
+    H, rows = 28672, 331
+    d = synth.sln_inputs((rows, H), None, "f32", has_beta=True, has_bias=True, seed=H + 5)
+    o = oracle.skip_layer_norm(d["input"], d["skip"], d["gamma"], d["beta"], d["bias"], d["epsilon"])
+    want_sum = oracle.skip_bias_sum(d["input"], d["skip"], d["bias"])
+    for _ in range(8):
+        out, s = run(lib, d, residual=True)
+        assert_norm_close(out.reshape(-1, H), o["output"].reshape(-1, H), torch.float32)
+        assert_bit_exact(s.reshape(-1, H), want_sum.reshape(-1, H))
+
+
 @pytest.mark.parametrize("dtype,H,beta,bias,res,skip_rows", [
     ("f16", 32768, False, False, False, None), ("f32", 20480, True, False, False, 5),
     ("bf16", 24576, False, True, True, 7), ("f32", 32768, True, True, True, None),
