@@ -268,6 +268,8 @@ __global__ void __launch_bounds__(256) k_bias_softmax_packed(const SmKernelArgs 
 
 constexpr int kWsConsumers = 256;
 constexpr int kTmaMaxStages = 8;
+// CTAs of 257-416 consumer threads are sized to run two to an SM
+constexpr int kWide2Max = 416;
 
 // EXACT: the row is exactly TPR*NV fragments, so no column needs a bounds check.
 // PARTS > 1 (one 256-thread row a tile, exact, NV a multiple of PARTS): a tile
@@ -276,7 +278,7 @@ constexpr int kTmaMaxStages = 8;
 // that stages stay small and two CTAs fit on an SM.  A lane's fragments
 // v in [p NV/PARTS, (p+1) NV/PARTS) lie in part p.
 template <typename T, int TPR, int NV, bool EXACT, int PARTS = 1, int NC = kWsConsumers>
-__global__ void __launch_bounds__(NC + 32, NC > kWsConsumers ? 1 : EP_SM_TMA_MIN_CTAS)
+__global__ void __launch_bounds__(NC + 32, NC > kWsConsumers ? (NC <= kWide2Max ? 2 : 1) : EP_SM_TMA_MIN_CTAS)
 k_bias_softmax_rows_tma(const SmKernelArgs a, int stages, int bias_slots, int64_t ntiles) {
   constexpr int VW = dev::Vec16<T>::N;
   constexpr int RT = NC / TPR;
@@ -1150,20 +1152,45 @@ TmaRowFn wide_row_kernel() {
   return k_bias_softmax_rows_tma<T, kWideTpr, NV, true, (NV % 2 == 0 ? NV / 2 : NV), kWideTpr>;
 }
 
-// 16-bit rows of 18432-30720 columns (multiples of 2048): 4 fragments a
-// thread on nfrag / 4 consumer threads (576-960, whole warps), the row staged
-// in halves.  Against 512 threads holding 5-7 fragments each, the extra warps
-// hide more of each row's reductions: 0.50-0.62 of the copy bandwidth became
-// 0.65-0.73 (rows of 24576 and 32768, which 512 threads cover with 6 and 8
-// fragments, measured the same either way; four parts a row measured slower).
+// 16-bit rows of 28672 and 30720 columns (and, without EP_SM_WIDE_2CTA, every
+// multiple of 2048 from 18432): 4 fragments a thread on nfrag / 4 consumer
+// threads (576-960, whole warps), the row staged in halves.  Against 512
+// threads holding 5-7 fragments each, the extra warps hide more of each row's
+// reductions: 0.50-0.62 of the copy bandwidth became 0.65-0.73 (rows of 24576
+// and 32768, which 512 threads cover with 6 and 8 fragments, measured the same
+// either way; four parts a row measured slower).
 template <typename T, int TPR>
 TmaRowFn wide4_row_kernel() {
   return k_bias_softmax_rows_tma<T, TPR, 4, true, 2, TPR>;
 }
 
+// 16-bit rows of 18432-26624 columns (multiples of 2048): 8 fragments a
+// thread on nfrag / 8 threads (288-416), two CTAs an SM, the row staged in
+// quarters: one CTA's reductions and exponent phase overlap the other's, which
+// one row at a time on one CTA could not hide (0.76-0.79 -> 0.83-0.88 of the
+// copy bandwidth against nfrag/4 threads of 4 fragments).  Wider rows would
+// need more than 80 registers a thread at two CTAs an SM, and spilled
+// (28672-30720: 0.51-0.55).
+template <typename T, int TPR>
+TmaRowFn wide8_row_kernel() {
+  return k_bias_softmax_rows_tma<T, TPR, 8, true, 4, TPR>;
+}
+
 template <typename T>
 TmaRowFn pick_wide4_row_kernel(int64_t nfrag, int* parts, int* consumers) {
   if (nfrag % 256 != 0) return nullptr;
+  if (EP_SM_WIDE_2CTA) {
+    *parts = 4;
+    *consumers = static_cast<int>(nfrag / 8);
+    switch (nfrag / 8) {
+      case 288: return wide8_row_kernel<T, 288>();
+      case 320: return wide8_row_kernel<T, 320>();
+      case 352: return wide8_row_kernel<T, 352>();
+      case 384: return wide8_row_kernel<T, 384>();
+      case 416: return wide8_row_kernel<T, 416>();
+      default: break;
+    }
+  }
   *parts = 2;
   *consumers = static_cast<int>(nfrag / 4);
   switch (nfrag / 4) {
@@ -1298,7 +1325,8 @@ bool launch_tma_rows(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_count, 
   int stages = std::min<int>(kTmaMaxStages, std::max<int>(parts > 1 ? 3 : 2, kTmaStageBudget / stage_bytes));
   // the 512-thread CTAs fill the register file and run alone on their SM:
   // as many stages as fit
-  if (consumers > kWsConsumers) stages = std::min<int>(kTmaMaxStages, int((224u * 1024u) / stage_bytes));
+  if (consumers > kWsConsumers)
+    stages = std::min<int>(kTmaMaxStages, int((consumers <= kWide2Max ? 112u * 1024u : 224u * 1024u) / stage_bytes));
   const size_t smem = size_t(stages) * stage_bytes;
   const int threads = consumers + 32;
   int per_sm = 1;

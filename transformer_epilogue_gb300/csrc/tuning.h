@@ -90,6 +90,11 @@
 #endif
 // 1: staged softmax rows of 16-bit types form the exponent with one packed
 // fused multiply-add per pair of elements.
+// 1: 16-bit rows of 18432-26624 columns take 8 fragments a thread on nfrag/8
+// threads, two CTAs an SM (0: nfrag/4 threads of 4 fragments, one CTA).
+#ifndef EP_SM_WIDE_2CTA
+#define EP_SM_WIDE_2CTA 1
+#endif
 #ifndef EP_SM_LEAN16
 #define EP_SM_LEAN16 1
 #endif
