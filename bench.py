@@ -72,8 +72,8 @@ ORDER = [
 
 # DRAM bytes (read + write) per launch from ncu captures of each kernel alone
 # (`--profile NAME`: one workload, a few launches), keyed by workload, with the
-# hash of the kernel sources they were taken on.  A changed source makes the
-# figure stale and it is reported as null.  ncu flushes L2 before each launch,
+# hash of the kernel sources' code (comments excluded) they were taken on.  A
+# changed source makes the figure stale and it is reported as null.  ncu flushes L2 before each launch,
 # so reads are cold (the split-row softmax: pass 2 re-reads from DRAM what a
 # step serves from L2), and writes still dirty in L2 when a kernel ends are not
 # counted.
@@ -87,15 +87,40 @@ NCU_TRAFFIC = {
     "sln_f32_2x128x768": 1608960,
     "sln_f32_32x2048x1024_bcast_skip": 488529664,
 }
-NCU_TRAFFIC_SOURCE_HASH = "0b71a783e10bdebf"
+NCU_TRAFFIC_SOURCE_HASH = "24ff61884dc1d62d"
+
+
+def _code_only(text: str) -> str:
+    """C/C++ source without its comments and blank lines (string and character
+    literals kept), so that a comment-only edit leaves the hash unchanged."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code (comments excluded)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "transformer_epilogue_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h", ".cpp")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+            h.update(_code_only(open(os.path.join(csrc, f), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1141,11 +1141,12 @@ inline int exact_tpr(int64_t nfrag, int nv) {
   return (t >= 4 && t <= 256 && (t & (t - 1)) == 0) ? static_cast<int>(t) : 0;
 }
 
-// Rows of 16385-32768 columns that 512 threads cover exactly (16-bit rows of
-// 20480, 24576, 28672 and 32768; float32 rows of every multiple of 2048): one
-// row a tile on 512 consumer threads holding NV fragments each (40-64
-// floats), staged with its bias row in NV/2 parts of 16 KB (NV odd: NV parts of
-// 8 KB); the CTA runs alone on its SM and takes as many stages as fit.
+// Rows of 16385-32768 columns that 512 threads cover exactly and that the
+// shapes below do not take (16-bit rows of 32768, and of 20480-28672 when those
+// are switched off; float32 rows of every multiple of 2048): one row a tile on
+// 512 consumer threads holding NV fragments each (40-64 floats), staged with
+// its bias row in NV/2 parts of 16 KB (NV odd: NV parts of 8 KB); the CTA runs
+// alone on its SM and takes as many stages as fit.
 constexpr int kWideTpr = 512;
 template <typename T, int NV>
 TmaRowFn wide_row_kernel() {
@@ -1323,8 +1324,8 @@ bool launch_tma_rows(const SmKernelArgs& k, const SoftmaxArgs& a, int sm_count, 
   const uint32_t stage_bytes = uint32_t(rt + slots) * row_bytes;
   if (2 * stage_bytes > 2 * kTmaStageBudget) return false;
   int stages = std::min<int>(kTmaMaxStages, std::max<int>(parts > 1 ? 3 : 2, kTmaStageBudget / stage_bytes));
-  // the 512-thread CTAs fill the register file and run alone on their SM:
-  // as many stages as fit
+  // wide-row CTAs (more than 256 consumers) run alone on their SM, or two to
+  // an SM up to kWide2Max consumers: as many stages as fit in their share
   if (consumers > kWsConsumers)
     stages = std::min<int>(kTmaMaxStages, int((consumers <= kWide2Max ? 112u * 1024u : 224u * 1024u) / stage_bytes));
   const size_t smem = size_t(stages) * stage_bytes;

@@ -675,9 +675,10 @@ inline int exact_tpr(int64_t nfrag, int nv) {
   return (t >= 4 && t <= 256 && (t & (t - 1)) == 0) ? static_cast<int>(t) : 0;
 }
 
-// Rows of 16385-32768 elements that 512 threads cover exactly (16-bit rows of
-// 20480, 24576, 28672 and 32768; float32 rows of every multiple of 2048): one
-// row a tile on 512 consumer threads holding NV fragments each (40-64 floats),
+// Rows of 16385-32768 elements that 512 threads cover exactly and that the
+// shapes below do not take (16-bit rows of 24576 and 32768; float32 rows of
+// every multiple of 2048 up to 24576, and 32768): one row a tile on 512
+// consumer threads holding NV fragments each (40-64 floats),
 // staged in NV/2 parts of 16 KB (NV odd: NV parts of 8 KB), gamma/beta/bias
 // through the read-only path; the CTA runs alone on its SM and takes as many
 // stages as fit, so the next row streams in while the consumers reduce and
@@ -858,8 +859,8 @@ cudaError_t launch_t(const SlnArgs& a, int sm_count, cudaStream_t stream, int* l
       const uint32_t stage_bytes = 2u * uint32_t(rt) * row_bytes / uint32_t(parts);
       const uint32_t param_stride = (row_bytes + 127u) / 128u * 128u;
       uint32_t param_bytes = parts > 1 ? 0u : param_stride * (1u + (a.beta != nullptr) + (a.bias != nullptr));
-      // 16-bit 512-thread rows: gamma and beta in shared memory (they fit
-      // beside three stages up to 32768 elements)
+      // 16-bit wide rows (more than 256 consumers): gamma and beta in shared
+      // memory (they fit beside three stages up to 32768 elements)
       uint32_t pstride = param_stride;
       if (parts > 1) {
         const uint32_t gb = param_stride * (1u + (a.beta != nullptr));
@@ -873,7 +874,7 @@ cudaError_t launch_t(const SlnArgs& a, int sm_count, cudaStream_t stream, int* l
       // A CTA whose parameters and two stages already exceed half of shared
       // memory, or whose threads fill the register file, runs alone on its SM:
       // give it as many stages as fit, so that more rows are in flight (f16
-      // H = 10240-12288, f32 H = 5120-6144, and the 512-thread wide rows).
+      // H = 10240-12288, f32 H = 5120-6144, and the wide rows).
       constexpr uint32_t kSmemForStages = 224u * 1024u;
       const bool alone = consumers > kWsConsumers ||
                          (param_bytes + 2u * stage_bytes > kSmemForStages / 2 &&

@@ -30,8 +30,9 @@
 #ifndef EP_SLN_TMA
 #define EP_SLN_TMA 1
 #endif
-// 1: rows of 16385-32768 elements that 512 threads cover exactly take the
-// staged kernel with 512 consumer threads (0: the 1024-thread register rows).
+// 1: rows of 16385-32768 elements take the staged kernel with more than 256
+// consumer threads where a wide shape covers them exactly (0: the 1024-thread
+// register rows).
 #ifndef EP_SLN_WIDE
 #define EP_SLN_WIDE 1
 #endif
@@ -78,8 +79,9 @@
 #ifndef EP_SM_CLC
 #define EP_SM_CLC 1
 #endif
-// 1: rows of 16385-32768 columns that 512 threads cover exactly take the
-// staged row kernel with 512 consumer threads (0: the split-row pair).
+// 1: rows of 16385-32768 columns take the staged row kernel with more than 256
+// consumer threads where a wide shape covers them exactly (0: the split-row
+// pair).
 #ifndef EP_SM_WIDE
 #define EP_SM_WIDE 1
 #endif
