@@ -38,7 +38,8 @@
  *  - Pointers must be aligned to sizeof(T).  16-byte alignment is not
  *    required: it selects the 128-bit vector path (BiasAdd and QuickGelu also
  *    when X, skip and Y share one offset within 16 bytes), and other alignments
- *    take a scalar path with the same results.
+ *    take a scalar path computing the same function (the results agree within
+ *    the ops' tolerances).
  *  - An output may alias an input exactly (same address, same size: in place).
  *    Any other overlap between an output and another operand is rejected.
  *  - Counts and offsets are 64-bit.
